@@ -1,0 +1,390 @@
+"""Benchmark: exact attention forward on GB300, through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one attention forward over the bf16 causal workload B=4, H=16, N=2048, d=128
+(scale 1/sqrt(128)), O in bf16 and lse in fp32, inputs resident in HBM.  value = algorithmic
+TFLOP/s: 2*(dk + dv) FLOPs per visible (query, key) pair, causal pairs only, divided by the
+device time of the step (CUDA events on the launching stream; L2 flushed before every timed
+step by writing a 256 MiB buffer outside the timed interval).  The same line carries:
+  e2e           the same metric with the step's inputs copied host->device from pinned memory
+                and o, lse copied back inside the timed interval;
+  roofline      the fused kernel's achieved TFLOP/s against the measured dense-bf16 peak;
+  decode        split-KV decode on B=64, H=32, L=8192 (kv_len ~ U{1..8192}), d=128, 16 splits:
+                KV GB/s (visible keys only) against the measured HBM peak;
+  cpu_baseline  the float64 CPU oracle timed on a bounded sample of the same workload;
+  clocks        SM clocks sampled with nvidia-smi during the timed region.
+Under torchrun (N > 1) every rank runs its own replica (weak scaling, no collective on the data
+path); value = total FLOPs of all ranks / the slowest rank's time.
+
+--impl reference times the float64 CPU oracle (the only reference there is: the pages publish
+no GPU kernel) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (prefill) and KV-read GB/s (decode) on 1 GB300, % of roofline"
+WORKLOAD = "bf16_causal_b4_h16_n2048_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha(name):
+    with open(os.path.join(ROOT, "online_softmax_fa2_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(summary, source):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    m = re.search(r"<!--\s*bench:\s*(\{.*?\})\s*-->", open(path).read(), re.S)
+    if not m:
+        return None
+    d = json.loads(m.group(1))
+    if d.get("source_sha256") != kernel_sha(source):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)  # nvidia-smi needs a moment before its first sample
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, ln in self.lines:
+            if not (t0 - 0.05 <= t <= t1 + 0.05):
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(a, seconds_target, seed=0):
+    """Time the float64 oracle on whole heads of workload `a` (taken in a fixed seeded order)
+    until about `seconds_target` of CPU work; returns (TFLOP/s, sample description, threads)."""
+    import numpy as np
+    import torch
+    import oracle
+
+    q = a.q.detach().cpu().float()
+    k = a.k.detach().cpu().float()
+    v = a.v.detach().cpu().float()
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(a.B * a.H)
+    flops_head = a.flops() / (a.B * a.H)
+    done, t_used, threads = 0, 0.0, 0
+    for bh in order:
+        b, h = divmod(int(bh), a.H)
+        t0 = time.perf_counter()
+        _, _, threads = oracle.attn_fwd(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, h:h + 1],
+                                        v[b:b + 1, :, h:h + 1], causal=a.causal, scale=a.scale)
+        t_used += time.perf_counter() - t0
+        done += 1
+        if t_used >= seconds_target:
+            break
+    return (done * flops_head / t_used / 1e12, t_used,
+            f"{done} of {a.B * a.H} (b, h) heads, full causal rows, float64", threads, done)
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is one (b, h) head of the workload."""
+    import torch
+    from online_softmax_fa2_gb300 import workloads as wl
+    import oracle
+
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    a = wl.causal_2k("cpu")
+    q, k, v = a.q.float(), a.k.float(), a.v.float()
+    flops_head = a.flops() / (a.B * a.H)
+    # one head per step keeps --steps K --warmup W within minutes on the host cores
+    heads = [(i % a.B, (i * 7) % a.H) for i in range(args.steps + args.warmup)]
+    times, threads = [], 0
+    for n, (b, h) in enumerate(heads):
+        t0 = time.perf_counter()
+        _, _, threads = oracle.attn_fwd(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, h:h + 1],
+                                        v[b:b + 1, :, h:h + 1], causal=True, scale=a.scale)
+        dt = time.perf_counter() - t0
+        if n >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    val = flops_head / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step": "one (b, h) head of the workload per step",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": "one (b, h) head (2048 causal rows) per step"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import online_softmax_fa2_gb300 as ofa
+    from online_softmax_fa2_gb300 import workloads as wl
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ofa.load()
+    pk, pk_kind = peaks()
+    stream = torch.cuda.current_stream()
+
+    a = wl.causal_2k(dev)
+    flops = a.flops()
+    o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
+    lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ofa.device_error_flags()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    barrier()
+    t0 = time.time()
+    for s, e in ev:
+        flush.zero_()            # L2 flush, outside the timed interval
+        s.record(stream)
+        step()
+        e.record(stream)
+    barrier()
+    t1 = time.time()
+    clocks = clk.stop(t0, t1)
+    ms_steps = [s.elapsed_time(e) for s, e in ev]
+    ms = sum(ms_steps) / len(ms_steps)
+    if ofa.device_error_flags() & 1:
+        raise RuntimeError("a kernel gave up a bounded wait during the timed region")
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * flops / (ms / 1e3) / 1e12
+    achieved = flops / (ms / 1e3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, o and lse out, every step
+    hq = a.q.cpu().pin_memory()
+    hk = a.k.cpu().pin_memory()
+    hv = a.v.cpu().pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ofa.attn_fwd(dq, dk, dv, causal=True, scale=a.scale, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    n_e2e = max(5, min(args.steps, 50))
+    barrier()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    ee.record(stream)
+    barrier()
+    ms_e2e = es.elapsed_time(ee) / n_e2e
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    del dq, dk, dv, hq, hk, hv
+
+    # split-KV decode on the long-cache workload (its own roofline: HBM)
+    dec = None
+    if not args.no_decode:
+        d = wl.decode(dev)
+        ws = torch.empty(ofa.decode_workspace_bytes(d.B, d.H, d.dv, d.num_splits) // 4,
+                         dtype=torch.float32, device=dev)
+        od = torch.empty((d.B, 1, d.H, d.dv), dtype=d.q.dtype, device=dev)
+        ld = torch.empty((d.B, d.H, 1), dtype=torch.float32, device=dev)
+
+        def dstep():
+            ofa.attn_decode_splitkv(d.q, d.k, d.v, kv_lens=d.kv_lens, num_splits=d.num_splits,
+                                    scale=d.scale, workspace=ws, out=od, lse=ld)
+
+        for _ in range(max(3, args.warmup)):
+            dstep()
+        nd = max(5, min(args.steps, 100))
+        barrier()
+        ds, de = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ds.record(stream)
+        for _ in range(nd):       # the 8.6 GB cache is far larger than L2: no flush needed
+            dstep()
+        de.record(stream)
+        barrier()
+        ms_d = ds.elapsed_time(de) / nd
+        gbs = d.kv_bytes() / (ms_d / 1e3) / 1e9
+        dec = {"workload": "bf16_decode_b64_h32_l8192_d128_splits16", "value": gbs,
+               "unit": "GB/s", "ms_per_step": ms_d, "steps": nd,
+               "kv_bytes_per_step": d.kv_bytes(), "gpu_launches_per_step": 2,
+               "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                            "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                            "peak_kind": f"{pk_kind} copy bandwidth",
+                            "traffic": profiled_traffic("decode_split_kernel.decode_b64_h32_l8192_d128.md",
+                                                        "decode.cu")}}
+        del d, ws
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": a.B, "H": a.H, "N": a.Nq, "d": a.dk,
+                   "causal": True, "flops_per_step": flops, "l2": "flushed before every step",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps,
+        "e2e": {"value": world * flops / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                     "peak_kind": f"{pk_kind} dense bf16 (burst)",
+                     "traffic": profiled_traffic("fwd_bf16_kernel.causal_b4_h16_n2048_d128.md",
+                                                 "fwd_bf16_sm103.cu")},
+        "clocks": clocks,
+    }
+    if dec:
+        line["decode"] = dec
+    if rank == 0 and not args.no_cpu:
+        val, secs, sample, threads, nheads = cpu_oracle_sample(a, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": sample, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

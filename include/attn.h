@@ -1,0 +1,187 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact scaled-dot-product attention,
+ *
+ *     x_ij = scale * <q_i, k_j> + b_ij        for j in J_i (the visible keys of row i)
+ *     o_i  = sum_j exp(x_ij - m_i) v_j / l_i,  m_i = max_j x_ij,  l_i = sum_j exp(x_ij - m_i)
+ *     lse_i = m_i + ln l_i
+ *
+ * tile by tile with the mergeable per-row state (m, l, u): a running maximum, the
+ * exponential sum measured against it and the unnormalised value sum, both rescaled by
+ * exp(m_old - m_new) when the maximum grows, and divided once per row at the end.
+ *
+ * Sources (page title, then section / step / figure):
+ *   "How Does FlashAttention Preserve Global Softmax Across Tiles?"
+ *       section 1  the operator, visible set J_i, fixed bias b_ij, d_k != d_v allowed,
+ *                  scale independent of tile size;
+ *       section 3  the state (m, l, u) and the merge of disjoint key subsets;
+ *       section 5  tile loop, rows keep their own state, divide once at the end;
+ *       section 6  global positions; causal masks align the two sequences' ends
+ *                  ("bottom-right"); an entirely empty row returns zero;
+ *       section 7  the saved log-sum-exp L_i;
+ *       section 8  decode (one query row, a long key/value cache) split over the keys,
+ *                  the partial states merged.
+ *   "Flash attention and efficient attention: Visual walkthrough", Steps 4-5 (the three
+ *       running numbers; re-basing a sum to a new maximum by one multiply).
+ *   "Reducing Memory Traffic with Output Accumulation in FlashAttention", Figures 1-3
+ *       (value-weighted sum first, both accumulators rescaled, one division).
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; it must stay valid until
+ *     the work queued on `stream` has finished.  The library keeps no pointer after a call
+ *     returns and allocates no device memory.
+ *   - All work is queued asynchronously on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) on the current CUDA device.
+ *   - Arguments are checked on the host before anything is queued; a bad argument returns a
+ *     non-zero attn_status_t and queues nothing.  attn_last_error() then describes it.
+ *     No entry point throws or aborts.
+ *   - Visible set J_i of query row i of batch entry b, with n_b = kv_lens[b] clamped to
+ *     [0, Nk] (Nk when kv_lens is NULL):  j < n_b, and, when causal,
+ *     j <= i + n_b - Nq (bottom-right alignment), and b_ij != -inf.
+ *     Nothing stored at a masked position is ever used: NaN there cannot reach an output.
+ *   - An empty row (J_i empty) gives o_i = +0.0 and lse_i = -inf, exactly.
+ *   - Accumulation is fp32.  bf16 outputs are rounded to nearest even once, at the end.
+ */
+#ifndef ONLINE_SOFTMAX_FA2_GB300_ATTN_H
+#define ONLINE_SOFTMAX_FA2_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad stride, bad scale */
+    ATTN_ERR_UNSUPPORTED = 2,    /* valid, but this build has no kernel for it (e.g. head dim) */
+    ATTN_ERR_MISALIGNED = 3,     /* a pointer or stride breaks the 16-byte rule of the path */
+    ATTN_ERR_CUDA = 4,           /* a CUDA runtime call or a launch failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (see attn_device_error_flags) */
+    ATTN_ERR_WORKSPACE = 6       /* the workspace is missing, misaligned or too small */
+} attn_status_t;
+
+typedef enum {
+    ATTN_DTYPE_F32 = 0,   /* q, k, v, o are float32 */
+    ATTN_DTYPE_BF16 = 1   /* q, k, v, o are bfloat16 */
+} attn_dtype_t;
+
+/*
+ * Arguments of one attention forward.
+ *
+ *   q  [B, Nq, H, dk]   element (b, i, h, c) at q + b*q_stride[0] + i*q_stride[1]
+ *                       + h*q_stride[2] + c          (strides in ELEMENTS; c contiguous)
+ *   k  [B, Nk, H, dk]   same with k_stride;  v [B, Nk, H, dv] with v_stride
+ *   o  [B, Nq, H, dv]   written, with o_stride
+ *   lse [B, H, Nq]      fp32, contiguous, written; may be NULL
+ *   bias                NULL, or fp32 b_ij of (b, h, i, j) at
+ *                       bias + b*bias_stride[0] + h*bias_stride[1] + i*bias_stride[2] + j;
+ *                       a stride of 0 broadcasts; -inf masks the position; bias is added
+ *                       after scaling and is not scaled
+ *   kv_lens             NULL, or device int32 [B]: keys j >= kv_lens[b] are padding
+ *   causal              0: no causal mask; 1: bottom-right causal mask
+ *   scale               multiplies <q_i, k_j>; the standard operator uses 1/sqrt(dk)
+ *   block_k             float32 path only: key tile size 16, 32 or 64 (0 picks 64);
+ *                       must be 0 for bfloat16
+ *
+ * bfloat16 path (tcgen05 tensor cores): dk in {64, 128, 192}, dv in {64, 128},
+ *   scale > 0; q, k, v base pointers 16-byte aligned and their b, n, h strides multiples of
+ *   8 elements (16 bytes).
+ * float32 path (exact fp32 SIMT): 1 <= dk, dv <= 256; any finite scale.
+ */
+typedef struct {
+    int32_t dtype;           /* attn_dtype_t */
+    int32_t causal;          /* 0 or 1 */
+    int64_t B, H, Nq, Nk, dk, dv;
+    const void *q;
+    const void *k;
+    const void *v;
+    void *o;
+    int64_t q_stride[3];     /* b, n, h */
+    int64_t k_stride[3];
+    int64_t v_stride[3];
+    int64_t o_stride[3];
+    float *lse;
+    const float *bias;
+    int64_t bias_stride[3];  /* b, h, i (j stride is 1) */
+    const int32_t *kv_lens;
+    float scale;
+    int32_t block_k;
+} attn_fwd_params_t;
+
+/*
+ * attn_fwd -- O and lse of exact attention for every (b, h, i).
+ * ("How Does FlashAttention Preserve Global Softmax Across Tiles?", sections 1, 5, 6, 7.)
+ * Queues one kernel.  Nq == 0 or B*H == 0 queues nothing and returns ATTN_OK.  Nk == 0 is
+ * legal (every row is empty; k and v may then be NULL).
+ */
+attn_status_t attn_fwd(const attn_fwd_params_t *params, attn_stream_t stream);
+
+/*
+ * Size in bytes of the workspace attn_decode_splitkv needs: the per-split partial states,
+ * float32 [B, H, num_splits, 2 + dv] laid out (m, l, u[0..dv)), where m is the maximum
+ * logit of the split (natural-log units), l = sum exp(x_j - m) and u = sum exp(x_j - m) v_j
+ * over the split's visible keys; an empty split is (-inf, 0, 0...).
+ */
+size_t attn_decode_workspace_bytes(int64_t B, int64_t H, int64_t dv, int32_t num_splits);
+
+/*
+ * attn_decode_splitkv -- one query row per (b, h) (params->Nq must be 1) against a long
+ * key/value cache, the keys of each sequence split into num_splits contiguous near-equal
+ * ranges of [0, n_b) (split s covers [floor(s*n_b/S), floor((s+1)*n_b/S))).
+ * ("How Does FlashAttention Preserve Global Softmax Across Tiles?", section 8, decode;
+ *  section 3, merge.)
+ * Queues two kernels on `stream`: the split kernel writes every partial state into
+ * `workspace` (layout above), then the merge kernel writes o and lse exactly as attn_fwd
+ * would.  The workspace is caller-owned device memory of at least
+ * attn_decode_workspace_bytes(...) bytes, 16-byte aligned; after the call it holds the
+ * partial states.  Supported: bfloat16, dk == dv in {64, 128}, 1 <= num_splits <= 256.
+ * The cache may use any strides that keep each key row contiguous and 16-byte aligned
+ * (e.g. a [B, H, L, d] cache passed with k_stride = {H*L*d, d, L*d}).
+ */
+attn_status_t attn_decode_splitkv(const attn_fwd_params_t *params, int32_t num_splits,
+                                  void *workspace, size_t workspace_bytes,
+                                  attn_stream_t stream);
+
+/*
+ * attn_merge_states -- merge S partial states per (b, h) and finalise.
+ * ("How Does FlashAttention Preserve Global Softmax Across Tiles?", section 3: put both
+ *  maxima into the common maximum, scale l and u of each part by exp(m_s - m), add;
+ *  empty parts are skipped.  "Flash attention and efficient attention: Visual
+ *  walkthrough", Step 5.)
+ *   partials  device fp32 [B, H, S, 2 + dv] as (m, l, u); a part with l == 0 is empty
+ *   o         written: row (b, h) at o + b*o_stride[0] + h*o_stride[2] (o_stride[1] unused),
+ *             element type o_dtype; u/l, or +0.0 when every part is empty
+ *   lse       device fp32 [B, H] written: m + ln l, or -inf when every part is empty; may be
+ *             NULL
+ * Queues one kernel.
+ */
+attn_status_t attn_merge_states(const float *partials, int64_t B, int64_t H, int32_t num_splits,
+                                int64_t dv, int32_t o_dtype, void *o, const int64_t o_stride[3],
+                                float *lse, attn_stream_t stream);
+
+/* Message describing the last non-OK status returned on the calling thread ("" if none). */
+const char *attn_last_error(void);
+
+/*
+ * Device error word of the current device (synchronous: waits for the device to finish its
+ * queued work first).  Bit 0: a kernel gave up a bounded wait on an mbarrier and returned
+ * early (its outputs are then incomplete).  Bit 1: a kv_lens value was outside [0, Nk] and
+ * was clamped.  clear != 0 resets the word to 0 after reading.  Returns ATTN_OK or
+ * ATTN_ERR_CUDA.
+ */
+attn_status_t attn_device_error_flags(uint32_t *out, int32_t clear);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ONLINE_SOFTMAX_FA2_GB300_ATTN_H */

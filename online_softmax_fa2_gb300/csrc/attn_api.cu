@@ -1,0 +1,217 @@
+// attn_api.cu -- the C ABI: argument checks, dispatch to the kernels, error reporting.
+//
+// Every check happens here, on the host, before anything is queued; the launchers in the
+// other translation units assume valid arguments.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attn_internal.h"
+
+namespace attn {
+
+static thread_local char g_msg[512] = "";
+
+attn_status_t fail(attn_status_t st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+// The device error word: one per device, lives as long as the library is loaded.
+__device__ uint32_t g_device_flags;
+
+static constexpr int kMaxDevices = 64;
+static uint32_t *g_flag_addr[kMaxDevices];
+static int g_sm_count[kMaxDevices];
+static std::mutex g_dev_mutex;
+
+uint32_t *device_flags() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_flag_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_flags) != cudaSuccess) return nullptr;
+        g_flag_addr[dev] = static_cast<uint32_t *>(ptr);
+    }
+    return g_flag_addr[dev];
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static attn_status_t check_strides(const char *name, const int64_t s[3]) {
+    for (int i = 0; i < 3; ++i)
+        if (s[i] < 0) return fail(ATTN_ERR_INVALID_ARG, "%s_stride[%d] = %lld is negative", name,
+                                  i, (long long)s[i]);
+    return ATTN_OK;
+}
+
+// Checks shared by attn_fwd and attn_decode_splitkv.
+static attn_status_t check_common(const attn_fwd_params_t *p) {
+    if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+    if (p->dtype != ATTN_DTYPE_F32 && p->dtype != ATTN_DTYPE_BF16)
+        return fail(ATTN_ERR_INVALID_ARG, "dtype %d is not ATTN_DTYPE_F32 or ATTN_DTYPE_BF16",
+                    p->dtype);
+    if (p->causal != 0 && p->causal != 1)
+        return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", p->causal);
+    if (p->B < 0 || p->H < 0 || p->Nq < 0 || p->Nk < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%lld H=%lld Nq=%lld Nk=%lld)",
+                    (long long)p->B, (long long)p->H, (long long)p->Nq, (long long)p->Nk);
+    if (p->dk < 1 || p->dv < 1)
+        return fail(ATTN_ERR_INVALID_ARG, "head dims must be >= 1 (dk=%lld dv=%lld)",
+                    (long long)p->dk, (long long)p->dv);
+    if (p->Nk > INT32_MAX || p->Nq > INT32_MAX)
+        return fail(ATTN_ERR_UNSUPPORTED, "sequence lengths above 2^31-1 are not supported");
+    if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    attn_status_t st;
+    if ((st = check_strides("q", p->q_stride)) || (st = check_strides("k", p->k_stride)) ||
+        (st = check_strides("v", p->v_stride)) || (st = check_strides("o", p->o_stride)))
+        return st;
+    if (p->bias)
+        for (int i = 0; i < 3; ++i)
+            if (p->bias_stride[i] < 0)
+                return fail(ATTN_ERR_INVALID_ARG, "bias_stride[%d] is negative", i);
+    if (p->B * p->H * p->Nq == 0) return ATTN_OK;
+    if (!p->q || !p->o) return fail(ATTN_ERR_INVALID_ARG, "q or o is NULL");
+    if (p->Nk > 0 && (!p->k || !p->v))
+        return fail(ATTN_ERR_INVALID_ARG, "k or v is NULL while Nk = %lld", (long long)p->Nk);
+    return ATTN_OK;
+}
+
+static bool stride_mult(const int64_t s[3], int64_t m) {
+    return s[0] % m == 0 && s[1] % m == 0 && s[2] % m == 0;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" attn_status_t attn_fwd(const attn_fwd_params_t *p, attn_stream_t stream) {
+    g_msg[0] = 0;
+    attn_status_t st = check_common(p);
+    if (st) return st;
+    if (p->B * p->H * p->Nq == 0) return ATTN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p->dtype == ATTN_DTYPE_F32) {
+        if (p->dk > 256 || p->dv > 256)
+            return fail(ATTN_ERR_UNSUPPORTED, "float32 path supports dk, dv <= 256 (dk=%lld dv=%lld)",
+                        (long long)p->dk, (long long)p->dv);
+        if (p->block_k != 0 && p->block_k != 16 && p->block_k != 32 && p->block_k != 64)
+            return fail(ATTN_ERR_INVALID_ARG, "block_k must be 0, 16, 32 or 64 (got %d)",
+                        p->block_k);
+        return launch_fwd_f32(*p, s);
+    }
+    // bfloat16: tcgen05 tensor-core path
+    if (p->dk != 64 && p->dk != 128 && p->dk != 192)
+        return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path supports dk in {64, 128, 192} (got %lld)",
+                    (long long)p->dk);
+    if (p->dv != 64 && p->dv != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path supports dv in {64, 128} (got %lld)",
+                    (long long)p->dv);
+    if (!(p->scale > 0.0f))
+        return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path needs scale > 0 (got %g)", p->scale);
+    if (p->block_k != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "block_k must be 0 for bfloat16 (got %d)", p->block_k);
+    if (!aligned16(p->q) || !aligned16(p->o) || (p->Nk > 0 && (!aligned16(p->k) || !aligned16(p->v))))
+        return fail(ATTN_ERR_MISALIGNED, "q, k, v and o must be 16-byte aligned");
+    if (!stride_mult(p->q_stride, 8) || !stride_mult(p->k_stride, 8) ||
+        !stride_mult(p->v_stride, 8) || !stride_mult(p->o_stride, 8))
+        return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
+    if (p->bias && (!aligned16(p->bias) || p->bias_stride[0] % 4 || p->bias_stride[1] % 4 ||
+                    p->bias_stride[2] % 4))
+        return fail(ATTN_ERR_MISALIGNED,
+                    "bias must be 16-byte aligned with strides that are multiples of 4");
+    return launch_fwd_bf16(*p, s);
+}
+
+extern "C" size_t attn_decode_workspace_bytes(int64_t B, int64_t H, int64_t dv, int32_t num_splits) {
+    if (B < 0 || H < 0 || dv < 1 || num_splits < 1) return 0;
+    return (size_t)B * (size_t)H * (size_t)num_splits * (size_t)(2 + dv) * sizeof(float);
+}
+
+extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t num_splits,
+                                             void *workspace, size_t workspace_bytes,
+                                             attn_stream_t stream) {
+    g_msg[0] = 0;
+    attn_status_t st = check_common(p);
+    if (st) return st;
+    if (p->Nq != 1) return fail(ATTN_ERR_INVALID_ARG, "decode needs Nq == 1 (got %lld)", (long long)p->Nq);
+    if (num_splits < 1 || num_splits > 256)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [1, 256] (got %d)", num_splits);
+    if (p->dtype != ATTN_DTYPE_BF16)
+        return fail(ATTN_ERR_UNSUPPORTED, "decode supports bfloat16 only");
+    if (p->dk != p->dv || (p->dk != 64 && p->dk != 128))
+        return fail(ATTN_ERR_UNSUPPORTED, "decode supports dk == dv in {64, 128} (dk=%lld dv=%lld)",
+                    (long long)p->dk, (long long)p->dv);
+    if (p->B * p->H == 0) return ATTN_OK;
+    if (!aligned16(p->q) || !aligned16(p->o) || (p->Nk > 0 && (!aligned16(p->k) || !aligned16(p->v))))
+        return fail(ATTN_ERR_MISALIGNED, "q, k, v and o must be 16-byte aligned");
+    if (!stride_mult(p->q_stride, 8) || !stride_mult(p->k_stride, 8) ||
+        !stride_mult(p->v_stride, 8) || !stride_mult(p->o_stride, 8))
+        return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
+    size_t need = attn_decode_workspace_bytes(p->B, p->H, p->dv, num_splits);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)",
+                    need, workspace_bytes);
+    float *part = static_cast<float *>(workspace);
+    st = launch_decode_split(*p, num_splits, part, reinterpret_cast<cudaStream_t>(stream));
+    if (st) return st;
+    return launch_merge(part, p->B, p->H, num_splits, p->dv, p->dtype, p->o, p->o_stride, p->lse,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status_t attn_merge_states(const float *partials, int64_t B, int64_t H,
+                                           int32_t num_splits, int64_t dv, int32_t o_dtype,
+                                           void *o, const int64_t o_stride[3], float *lse,
+                                           attn_stream_t stream) {
+    g_msg[0] = 0;
+    if (B < 0 || H < 0) return fail(ATTN_ERR_INVALID_ARG, "negative B or H");
+    if (num_splits < 1 || num_splits > 4096)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [1, 4096] (got %d)", num_splits);
+    if (dv < 1 || dv > 1024) return fail(ATTN_ERR_UNSUPPORTED, "dv must be in [1, 1024]");
+    if (o_dtype != ATTN_DTYPE_F32 && o_dtype != ATTN_DTYPE_BF16)
+        return fail(ATTN_ERR_INVALID_ARG, "bad o_dtype %d", o_dtype);
+    if (B * H == 0) return ATTN_OK;
+    if (!partials || !o || !o_stride) return fail(ATTN_ERR_INVALID_ARG, "partials, o or o_stride is NULL");
+    for (int i = 0; i < 3; ++i)
+        if (o_stride[i] < 0) return fail(ATTN_ERR_INVALID_ARG, "o_stride[%d] is negative", i);
+    return launch_merge(partials, B, H, num_splits, dv, o_dtype, o, o_stride, lse,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" const char *attn_last_error(void) { return g_msg; }
+
+extern "C" attn_status_t attn_device_error_flags(uint32_t *out, int32_t clear) {
+    g_msg[0] = 0;
+    if (!out) return fail(ATTN_ERR_INVALID_ARG, "out is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    e = cudaMemcpyFromSymbol(out, g_device_flags, sizeof(uint32_t));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+    if (clear) {
+        uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_device_flags, &zero, sizeof(uint32_t));
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
+    }
+    return ATTN_OK;
+}
+
+extern "C" int32_t attn_version(void) { return 100; }

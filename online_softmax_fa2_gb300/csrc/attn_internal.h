@@ -1,0 +1,32 @@
+// attn_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Error bits of the device error word (see attn_device_error_flags).
+enum : uint32_t { kFlagWaitTimeout = 1u, kFlagKvLenClamped = 2u };
+
+// Records a message for attn_last_error() and returns `st`.
+attn_status_t fail(attn_status_t st, const char *fmt, ...);
+
+// Device address of the device error word of the current device (nullptr on failure).
+uint32_t *device_flags();
+
+// Launchers.  Arguments have been validated by the caller (attn_api.cu).
+attn_status_t launch_fwd_f32(const attn_fwd_params_t &p, cudaStream_t s);
+attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s);
+attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
+                                  cudaStream_t s);
+attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int num_splits,
+                           int64_t dv, int o_dtype, void *o, const int64_t o_stride[3],
+                           float *lse, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace attn

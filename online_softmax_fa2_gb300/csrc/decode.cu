@@ -1,0 +1,267 @@
+// decode.cu -- split-KV decode and the merge of partial (m, l, u) states.
+//
+// "How Does FlashAttention Preserve Global Softmax Across Tiles?", section 8: decode has one
+// query row against a long key/value cache, so the work is reading the cache.  The keys of
+// each sequence are split into S contiguous ranges; each range gives a partial state
+// (m, l, u) (section 3), and the partial states are merged by putting both maxima into the
+// common maximum and scaling l and u of each part by exp(m_s - m) before adding (section 3;
+// "Flash attention and efficient attention: Visual walkthrough", Step 5).  Empty parts are
+// skipped; a row whose parts are all empty gives o = +0.0, lse = -inf (section 6).
+//
+// Split kernel: grid (S, H, B), 128 threads.  The cache is read once, with 16-byte loads:
+// a group of D/8 lanes holds one key row (each lane 8 bf16 of K and 8 of V), so a warp
+// reads 32/(D/8) key rows per load instruction, coalesced.  Each group runs the online
+// update over its keys (key lo + g + t*G of the split for t = 0, 1, ..., G groups per CTA,
+// 4 keys in flight per group), with the logits kept in base-2 units (x * log2 e) so that one ex2
+// gives each exponential.  The G group states are then merged in shared memory and the
+// split's state is written in natural-log units.
+#include <cmath>
+
+#include <cuda_bf16.h>
+
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct DecArgs {
+    int B, H, Nk, S;
+    float scale_log2;
+    const __nv_bfloat16 *q, *k, *v;
+    long long qs0, qs2, ks0, ks1, ks2, vs0, vs1, vs2;
+    const float *bias;
+    long long bs0, bs1;
+    const int *kv_lens;
+    float *part;  // [B, H, S, 2 + D]
+    uint32_t *flags;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float f[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        f[2 * t] = __uint_as_float(w[t] << 16);
+        f[2 * t + 1] = __uint_as_float(w[t] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
+    constexpr int LPK = D / 8;            // lanes per key row
+    constexpr int G = kThreads / LPK;     // key groups per CTA
+    constexpr int U = 4;                  // keys in flight per group
+    __shared__ float sm_m[G], sm_l[G];
+    __shared__ float sm_u[G][D + 1];
+
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int g = threadIdx.x / LPK, sub = threadIdx.x % LPK, c0 = sub * 8;
+
+    int n = a.Nk;
+    if (a.kv_lens) {
+        int raw = a.kv_lens[b];
+        n = min(max(raw, 0), a.Nk);
+        if (raw != n && threadIdx.x == 0 && s == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
+    }
+    const int lo = (int)(((long long)s * n) / a.S), hi = (int)(((long long)(s + 1) * n) / a.S);
+
+    float qf[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.q + b * a.qs0 + h * a.qs2 + c0), qf);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) qf[t] *= a.scale_log2;
+
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks2 + c0;
+    const __nv_bfloat16 *vb = a.v + b * a.vs0 + h * a.vs2 + c0;
+    const float *bias_row = a.bias ? a.bias + b * a.bs0 + h * a.bs1 : nullptr;
+
+    float m = -INFINITY, l = 0.f, u[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) u[t] = 0.f;
+
+    // Every thread runs the same iterations (the shuffles below need the whole warp);
+    // key base + w*G + g belongs to group g.
+    for (int base = lo; base < hi; base += G * U) {
+        uint4 kr[U], vr[U];
+#pragma unroll
+        for (int w = 0; w < U; ++w) {
+            const int j = base + w * G + g;
+            kr[w] = make_uint4(0u, 0u, 0u, 0u);
+            vr[w] = kr[w];
+            if (j < hi) {
+                kr[w] = ld_stream(kb + (long long)j * a.ks1);
+                vr[w] = ld_stream(vb + (long long)j * a.vs1);
+            }
+        }
+        float x[U];
+#pragma unroll
+        for (int w = 0; w < U; ++w) {
+            float kf[8];
+            bf16x8_to_f32(kr[w], kf);
+            float d = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) d = fmaf(qf[t], kf[t], d);
+            x[w] = d;
+        }
+#pragma unroll
+        for (int w = 0; w < U; ++w) {
+#pragma unroll
+            for (int o = LPK / 2; o > 0; o >>= 1) x[w] += __shfl_xor_sync(0xffffffffu, x[w], o);
+        }
+#pragma unroll
+        for (int w = 0; w < U; ++w) {
+            const int j = base + w * G + g;
+            if (j >= hi) break;  // uniform across the group
+            float xs = x[w];
+            if (bias_row) {
+                float bj = bias_row[j];
+                if (bj == -INFINITY) continue;  // masked key
+                xs = fmaf(bj, kLog2e, xs);
+            }
+            float m_new = fmaxf(m, xs);
+            float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
+            float p = ex2(xs - m_new);
+            float vf[8];
+            bf16x8_to_f32(vr[w], vf);
+            l = fmaf(alpha, l, p);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) u[t] = fmaf(alpha, u[t], p * vf[t]);
+            m = m_new;
+        }
+    }
+
+    if (sub == 0) {
+        sm_m[g] = m;
+        sm_l[g] = l;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) sm_u[g][c0 + t] = u[t];
+    __syncthreads();
+
+    // merge the G group states; thread c owns column c
+    float M = -INFINITY;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg)
+        if (sm_l[gg] > 0.f) M = fmaxf(M, sm_m[gg]);
+    float *out = a.part + (((long long)b * a.H + h) * a.S + s) * (2 + D);
+    if (M == -INFINITY) {  // empty split
+        for (int c = threadIdx.x; c < D; c += kThreads) out[2 + c] = 0.f;
+        if (threadIdx.x == 0) {
+            out[0] = -INFINITY;
+            out[1] = 0.f;
+        }
+        return;
+    }
+    float L = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg)
+        if (sm_l[gg] > 0.f) L = fmaf(ex2(sm_m[gg] - M), sm_l[gg], L);
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+        float acc = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg)
+            if (sm_l[gg] > 0.f) acc = fmaf(ex2(sm_m[gg] - M), sm_u[gg][c], acc);
+        out[2 + c] = acc;
+    }
+    if (threadIdx.x == 0) {
+        out[0] = M * kLn2;  // back to natural-log units: exp(x - m) == 2^(x*log2e - M)
+        out[1] = L;
+    }
+}
+
+// Merge: one CTA per (b, h); thread t owns columns t, t + 128, ...
+template <typename OutT>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const float *part, int H, int S, int dv,
+                                                           OutT *o, long long os0, long long os2,
+                                                           float *lse) {
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const float *st = part + (long long)bh * S * (2 + dv);
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) {
+        const float l = st[s * (2 + dv) + 1];
+        if (l > 0.f) M = fmaxf(M, st[s * (2 + dv)]);
+    }
+    OutT *orow = o + b * os0 + h * os2;
+    if (M == -INFINITY) {
+        for (int c = threadIdx.x; c < dv; c += blockDim.x) orow[c] = OutT(0.f);
+        if (lse && threadIdx.x == 0) lse[bh] = -INFINITY;
+        return;
+    }
+    float L = 0.f;
+    for (int s = 0; s < S; ++s) {
+        const float l = st[s * (2 + dv) + 1];
+        if (l > 0.f) L = fmaf(expf(st[s * (2 + dv)] - M), l, L);
+    }
+    const float inv = 1.f / L;
+    for (int c = threadIdx.x; c < dv; c += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float *x = st + s * (2 + dv);
+            if (x[1] > 0.f) acc = fmaf(expf(x[0] - M), x[2 + c], acc);
+        }
+        orow[c] = OutT(acc * inv);
+    }
+    if (lse && threadIdx.x == 0) lse[bh] = M + logf(L);
+}
+
+}  // namespace
+
+attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
+                                  cudaStream_t st) {
+    DecArgs a;
+    a.B = (int)p.B; a.H = (int)p.H; a.Nk = (int)p.Nk; a.S = num_splits;
+    a.scale_log2 = p.scale * kLog2e;
+    a.q = static_cast<const __nv_bfloat16 *>(p.q);
+    a.k = static_cast<const __nv_bfloat16 *>(p.k);
+    a.v = static_cast<const __nv_bfloat16 *>(p.v);
+    a.qs0 = p.q_stride[0]; a.qs2 = p.q_stride[2];
+    a.ks0 = p.k_stride[0]; a.ks1 = p.k_stride[1]; a.ks2 = p.k_stride[2];
+    a.vs0 = p.v_stride[0]; a.vs1 = p.v_stride[1]; a.vs2 = p.v_stride[2];
+    a.bias = p.bias; a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1];
+    a.kv_lens = p.kv_lens; a.part = partials;
+    a.flags = device_flags();
+    if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
+    if (p.B > 65535 || p.H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "decode supports B, H <= 65535");
+    dim3 grid((unsigned)num_splits, (unsigned)p.H, (unsigned)p.B);
+    if (p.dk == 64) decode_split_kernel<64><<<grid, kThreads, 0, st>>>(a);
+    else decode_split_kernel<128><<<grid, kThreads, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int num_splits, int64_t dv,
+                           int o_dtype, void *o, const int64_t o_stride[3], float *lse,
+                           cudaStream_t st) {
+    if (B * H > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "B*H too large");
+    dim3 grid((unsigned)(B * H));
+    if (o_dtype == ATTN_DTYPE_BF16)
+        merge_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(partials, (int)H, num_splits, (int)dv,
+                                                               static_cast<__nv_bfloat16 *>(o),
+                                                               o_stride[0], o_stride[2], lse);
+    else
+        merge_kernel<float><<<grid, kThreads, 0, st>>>(partials, (int)H, num_splits, (int)dv,
+                                                       static_cast<float *>(o), o_stride[0],
+                                                       o_stride[2], lse);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+}  // namespace attn

@@ -1,0 +1,540 @@
+// fwd_bf16_sm103.cu -- fused bf16 attention forward on the 5th-generation tensor cores.
+//
+// One CTA computes one 128-row query tile of one (b, h) ("How Does FlashAttention Preserve
+// Global Softmax Across Tiles?", section 5: a tile of queries keeps its own per-row state
+// while key/value tiles stream past; section 8: query-block parallelism).  Work items are
+// numbered longest first (the last query tiles of a causal problem see the most keys), and
+// the hardware hands them to SMs as SMs free up.
+//
+// Roles (256 threads):
+//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage shared-memory ring
+//               (128-byte swizzled panels of 64 columns, the layout the tensor cores read).
+//   warp 1      tensor-core issuer (one thread): S_j = Q K_j^T into tensor memory (TMEM),
+//               double-buffered so S_{j+1} is computed while the softmax works on S_j, then
+//               O += P_j V_j with P_j read from TMEM.  Also owns the TMEM allocation.
+//   warps 4-7   softmax: thread t owns query row t (TMEM lane t), so row maxima and row sums
+//               need no shuffles.  Per key tile: load the row of S from TMEM, scale (and add
+//               the bias), mask in global positions, take the new maximum, form
+//               p = exp(x - m) with one ex2 per element, add to l, round P to bf16 into the
+//               TMEM columns S_j occupied, and signal the issuer.  At the end: o = u / l once,
+//               lse = m + ln l, empty rows o = +0.0 and lse = -inf.
+//
+// The (m, l, u) update follows "Reducing Memory Traffic with Output Accumulation in
+// FlashAttention" ("Rescaling Both Accumulators When the Maximum Increases"): when the
+// maximum grows, both l and the accumulator u (here the O columns in TMEM) are multiplied by
+// exp(m_old - m_new).  Rescaling is exact for any reference point shared by l and u, so a
+// row keeps its reference until the tile maximum exceeds it by more than 2^8 (then the
+// exponentials stay <= 256, far from fp32/bf16 overflow); rows therefore rescale O only a few
+// times in a whole pass instead of at every tile.
+//
+// Masking (section 6): key j of sequence b is visible to row i iff j < n_b and, when causal,
+// j <= i + n_b - Nq; a bias of -inf masks too.  Tiles past the last visible key are never
+// loaded.  Masked logits are selected to -inf (never multiplied), so NaN stored at a masked
+// position cannot reach the output; value rows past n_b inside the last tile are zeroed in
+// shared memory before the P V product (0 * NaN would otherwise be NaN).
+//
+// Every mbarrier wait is bounded (1 s of wall time): on expiry the thread raises a CTA-wide
+// abort flag and the device error word, every role leaves its loop, in-flight copies and
+// tensor-core work are waited for (again bounded), TMEM is freed and the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BQ = 128;            // query rows per tile (= MMA M = TMEM lanes)
+constexpr int BK = 128;            // keys per tile (= N of S = Q K^T, = K of O += P V)
+constexpr int kStages = 2;         // K/V shared-memory ring depth
+constexpr int kThreads = 256;
+constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes), 128B-swizzled
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units: keep the reference while x - m <= 8
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256;   // O accumulator columns [256, 256 + dv); S buffers at 0, 128
+
+struct Args {
+    int B, H, Nq, Nk, causal, n_qt;
+    float scale_log2;
+    __nv_bfloat16 *o;
+    long long os0, os1, os2;
+    float *lse;
+    const float *bias;
+    long long bs0, bs1, bs2;
+    const int *kv_lens;
+    uint32_t *flags;
+};
+
+struct Ctrl {
+    uint64_t q_full;
+    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t s_full[2], p_full[2];
+    uint64_t o_done;
+    uint64_t final_mma;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int DK, int DV>
+struct Layout {
+    static constexpr int kQBytes = (DK / 64) * kPanelBytes;
+    static constexpr int kKBytes = (DK / 64) * kPanelBytes;
+    static constexpr int kVBytes = (DV / 64) * kPanelBytes;
+    static constexpr int kStageBytes = kKBytes + kVBytes;
+    static constexpr int kDataBytes = kQBytes + kStages * kStageBytes;
+    static constexpr int kBytes = kDataBytes + (int)sizeof(Ctrl) + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ float max4(float a, float b, float c, float d) {
+    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+template <int DK, int DV, bool kBias>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Args a) {
+    using L = Layout<DK, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *sQ = smem;
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + L::kDataBytes);
+    volatile int *abort = &ctrl->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bhn = a.B * a.H;
+    const int qt = a.n_qt - 1 - (int)(blockIdx.x / bhn);  // longest first
+    const int bh = (int)(blockIdx.x % bhn), b = bh / a.H, h = bh % a.H;
+    const int q0 = qt * BQ;
+
+    int n = a.Nk;
+    if (a.kv_lens) {
+        const int raw = a.kv_lens[b];
+        n = min(max(raw, 0), a.Nk);
+        if (raw != n && threadIdx.x == 0 && qt == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
+    }
+    const int shift = n - a.Nq;  // causal: key j visible to row i iff j <= i + shift
+    int kv_end = n;
+    if (a.causal) kv_end = min(n, max(0, min(q0 + BQ, a.Nq) + shift));
+    const int n_tiles = (kv_end + BK - 1) / BK;
+
+    if (n_tiles == 0) {  // every row of this tile is empty: o = +0.0, lse = -inf
+        if (warp >= 4) {
+            const int i = q0 + (int)threadIdx.x - 128;
+            if (i < a.Nq) {
+                uint4 *orow = reinterpret_cast<uint4 *>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2);
+#pragma unroll
+                for (int c = 0; c < DV / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+                if (a.lse) a.lse[((long long)b * a.H + h) * a.Nq + i] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&ctrl->q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&ctrl->k_full[s], 1);
+            ptx::mbar_init(&ctrl->v_full[s], 1);
+            ptx::mbar_init(&ctrl->kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&ctrl->s_full[s], 1);
+            ptx::mbar_init(&ctrl->p_full[s], 128);
+        }
+        ptx::mbar_init(&ctrl->o_done, 1);
+        ptx::mbar_init(&ctrl->final_mma, 1);
+        ctrl->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&ctrl->tmem_base, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&ctrl->q_full, L::kQBytes);
+#pragma unroll
+            for (int p = 0; p < DK / 64; ++p)
+                ptx::tma_load_4d(sQ + p * kPanelBytes, &tm_q, &ctrl->q_full, p * 64, q0, h, b);
+            int last_issued = -1;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % kStages;
+                if (j >= kStages &&
+                    !ptx::mbar_wait(&ctrl->kv_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
+                                    kFlagWaitTimeout, kWaitLimitNs))
+                    break;
+                uint8_t *sK = smem + L::kQBytes + st * L::kStageBytes;
+                uint8_t *sV = sK + L::kKBytes;
+                ptx::mbar_arrive_expect_tx(&ctrl->k_full[st], L::kKBytes);
+#pragma unroll
+                for (int p = 0; p < DK / 64; ++p)
+                    ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[st], p * 64, j * BK, h, b);
+                ptx::mbar_arrive_expect_tx(&ctrl->v_full[st], L::kVBytes);
+#pragma unroll
+                for (int p = 0; p < DV / 64; ++p)
+                    ptx::tma_load_4d(sV + p * kPanelBytes, &tm_v, &ctrl->v_full[st], p * 64, j * BK, h, b);
+                last_issued = j;
+            }
+            if (*abort) {  // let copies still in flight land before the CTA exits
+                ptx::mbar_wait_quiet(&ctrl->q_full, 0, kWaitLimitNs);
+                for (int j = max(0, last_issued - kStages + 1); j <= last_issued; ++j) {
+                    const int st = j % kStages;
+                    ptx::mbar_wait_quiet(&ctrl->k_full[st], (j / kStages) & 1, kWaitLimitNs);
+                    ptx::mbar_wait_quiet(&ctrl->v_full[st], (j / kStages) & 1, kWaitLimitNs);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ tensor-core issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BQ, BK, false);
+            constexpr uint32_t kIdO = ptx::idesc_bf16_f32(BQ, DV, true);
+            const uint32_t q_addr = ptx::smem_u32(sQ);
+            bool ok = ptx::mbar_wait(&ctrl->q_full, 0, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % kStages, buf = j & 1;
+                if (!ptx::mbar_wait(&ctrl->k_full[st], (j / kStages) & 1, abort, a.flags,
+                                    kFlagWaitTimeout, kWaitLimitNs))
+                    return false;
+                ptx::tc_fence_after();
+                const uint32_t k_addr = ptx::smem_u32(smem + L::kQBytes + st * L::kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * kPanelBytes + (kk % 4) * 32;
+                    ptx::mma_ss(tmem + buf * BK, ptx::sdesc_sw128(q_addr + off, 16, 1024),
+                                ptx::sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&ctrl->s_full[buf]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles && !issue_s(j + 1)) break;
+                const int st = j % kStages, buf = j & 1;
+                if (!ptx::mbar_wait(&ctrl->p_full[buf], (j >> 1) & 1, abort, a.flags, kFlagWaitTimeout,
+                                    kWaitLimitNs))
+                    break;
+                if (!ptx::mbar_wait(&ctrl->v_full[st], (j / kStages) & 1, abort, a.flags,
+                                    kFlagWaitTimeout, kWaitLimitNs))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t v_addr =
+                    ptx::smem_u32(smem + L::kQBytes + st * L::kStageBytes + L::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    // P: bf16 pairs packed in TMEM columns (8 columns per 16 keys);
+                    // V: MN-major (dv contiguous), 8-key groups 1024 B apart, 64-column
+                    // panels kPanelBytes apart.
+                    ptx::mma_ts(tmem + kTmemO, tmem + buf * BK + kk * 8,
+                                ptx::sdesc_sw128(v_addr + kk * 16 * 128, kPanelBytes, 1024), kIdO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(&ctrl->o_done);
+                ptx::mma_commit(&ctrl->kv_empty[st]);
+            }
+            // all tensor-core work of this CTA done before TMEM is released
+            ptx::mma_commit(&ctrl->final_mma);
+            if (!ptx::mbar_wait_quiet(&ctrl->final_mma, 0, kWaitLimitNs)) atomicOr(a.flags, kFlagWaitTimeout);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int r = (int)threadIdx.x - 128;  // row in tile == TMEM lane
+        const int i = q0 + r;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        const float c = a.scale_log2;
+        const float* bias_row = nullptr;
+        if (kBias && i < a.Nq) bias_row = a.bias + b * a.bs0 + h * a.bs1 + (long long)i * a.bs2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        // every lane waits; the warp goes on only if all lanes succeeded (tcgen05.ld/st and
+        // the vote below are warp-collective, so the lanes must not part ways)
+        auto wait_warp = [&](uint64_t *bar, uint32_t parity) -> bool {
+            const bool w = ptx::mbar_wait(bar, parity, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
+            return __all_sync(0xffffffffu, w);
+        };
+
+        for (int j = 0; j < n_tiles; ++j) {
+            const int buf = j & 1, kv0 = j * BK;
+            if (!wait_warp(&ctrl->s_full[buf], (j >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            float x[BK];
+            {
+                uint32_t raw[BK];
+#pragma unroll
+                for (int cc = 0; cc < BK / 32; ++cc)
+                    ptx::tmem_ld32(lane_addr + buf * BK + cc * 32,
+                                   *reinterpret_cast<uint32_t(*)[32]>(&raw[cc * 32]));
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < BK / 32; ++cc)
+                    ptx::reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&raw[cc * 32]));
+#pragma unroll
+                for (int k = 0; k < BK; ++k) x[k] = __uint_as_float(raw[k]);
+            }
+            // logits in base-2 units; masked ones become -inf
+            const bool need_mask = (kv0 + BK > n) || (a.causal && kv0 + BK - 1 > q0 + shift);
+            if (kBias) {
+#pragma unroll
+                for (int k4 = 0; k4 < BK / 4; ++k4) {
+                    float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int key = kv0 + 4 * k4;
+                    if (bias_row && key + 3 < n)
+                        bb = __ldg(reinterpret_cast<const float4 *>(bias_row + key));
+                    else if (bias_row) {
+                        float t[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int e = 0; e < 4; ++e)
+                            if (key + e < n) t[e] = bias_row[key + e];
+                        bb = make_float4(t[0], t[1], t[2], t[3]);
+                    }
+                    x[4 * k4 + 0] = fmaf(x[4 * k4 + 0], c, bb.x * kLog2e);
+                    x[4 * k4 + 1] = fmaf(x[4 * k4 + 1], c, bb.y * kLog2e);
+                    x[4 * k4 + 2] = fmaf(x[4 * k4 + 2], c, bb.z * kLog2e);
+                    x[4 * k4 + 3] = fmaf(x[4 * k4 + 3], c, bb.w * kLog2e);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < BK; ++k) x[k] *= c;
+            }
+            if (need_mask) {
+                const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim visible
+#pragma unroll
+                for (int k = 0; k < BK; ++k)
+                    if (kv0 + k >= lim) x[k] = -INFINITY;
+            }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < BK; k += 4) mt = fmaxf(mt, max4(x[k], x[k + 1], x[k + 2], x[k + 3]));
+
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mt != -INFINITY) {
+                if (m_run == -INFINITY) {
+                    m_run = mt;  // first visible key: the old state has no mass
+                } else if (mt > m_run + kRescaleThreshold) {
+                    alpha = ptx::ex2(m_run - mt);
+                    m_run = mt;
+                    rescale = true;
+                }
+            }
+            const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+            float lsum = 0.f;
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                x[k] = ptx::ex2(x[k] - mref);
+                lsum += x[k];
+            }
+            l_run = fmaf(alpha, l_run, lsum);
+
+            // u <- alpha * u: rescale this warp's O rows once PV_{j-1} has landed
+            if (__any_sync(0xffffffffu, rescale)) {
+                if (!wait_warp(&ctrl->o_done, (j - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < DV / 32; ++cc) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld32(lane_addr + kTmemO + cc * 32, ov);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(ov);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+                    ptx::tmem_st32(lane_addr + kTmemO + cc * 32, ov);
+                }
+                ptx::tmem_st_wait();
+            }
+
+            // value rows past n inside this tile (still in bounds) may hold anything: zero them
+            if (kv0 + BK > n && n < a.Nk) {
+                const int st = j % kStages;
+                if (!wait_warp(&ctrl->v_full[st], (j / kStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int row = r;  // one key row per thread
+                if (kv0 + row >= n && kv0 + row < a.Nk) {
+                    uint8_t *sV = smem + L::kQBytes + st * L::kStageBytes + L::kKBytes;
+#pragma unroll
+                    for (int p = 0; p < DV / 64; ++p) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(sV + p * kPanelBytes + row * 128);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) dst[t] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+            }
+
+            // P (bf16) into the TMEM columns that held S_j
+#pragma unroll
+            for (int cc = 0; cc < BK / 64; ++cc) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) pk[t] = ptx::pack_bf16x2(x[cc * 64 + 2 * t], x[cc * 64 + 2 * t + 1]);
+                ptx::tmem_st32(lane_addr + buf * BK + cc * 32, pk);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&ctrl->p_full[buf]);
+        }
+
+        // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf
+        if (ok && wait_warp(&ctrl->o_done, (n_tiles - 1) & 1)) {
+            ptx::tc_fence_after();
+            const bool empty = !(l_run > 0.f);
+            const float inv = empty ? 0.f : 1.f / l_run;
+            uint4 *orow = (i < a.Nq)
+                              ? reinterpret_cast<uint4 *>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2)
+                              : nullptr;
+#pragma unroll
+            for (int cc = 0; cc < DV / 32; ++cc) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(lane_addr + kTmemO + cc * 32, ov);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(ov);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    pk[t] = empty ? 0u
+                                  : ptx::pack_bf16x2(__uint_as_float(ov[2 * t]) * inv,
+                                                     __uint_as_float(ov[2 * t + 1]) * inv);
+                if (orow) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        orow[cc * 4 + t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+                }
+            }
+            if (a.lse && i < a.Nq)
+                a.lse[((long long)b * a.H + h) * a.Nq + i] = empty ? -INFINITY : (m_run + log2f(l_run)) * kLn2;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D map over a [B, N, H, d] bf16 tensor with element strides s (b, n, h); box 64 x 128.
+attn_status_t encode(CUtensorMap *m, const void *ptr, int64_t B, int64_t N, int64_t H, int64_t d,
+                     const int64_t s[3], const char *name) {
+    auto enc = get_encoder();
+    if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    auto bstride = [](int64_t st, int64_t size) -> cuuint64_t {
+        return size <= 1 ? 16u : (cuuint64_t)(st * 2);  // stride of a size-1 dim is unused
+    };
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {bstride(s[1], N), bstride(s[2], H), bstride(s[0], B)};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "TMA descriptor for %s rejected (CUresult %d)", name, (int)r);
+    return ATTN_OK;
+}
+
+template <int DK, int DV, bool kBias>
+attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const Args &a,
+                       unsigned grid, cudaStream_t s) {
+    int smem = Layout<DK, DV>::kBytes;
+    if (smem < 116 * 1024) smem = 116 * 1024;  // one CTA per SM: it owns all 512 TMEM columns
+    auto kern = fwd_bf16_kernel<DK, DV, kBias>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16 launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+template <bool kBias>
+attn_status_t dispatch(int dk, int dv, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                       const Args &a, unsigned grid, cudaStream_t s) {
+    if (dk == 64 && dv == 64) return launch_t<64, 64, kBias>(mq, mk, mv, a, grid, s);
+    if (dk == 128 && dv == 128) return launch_t<128, 128, kBias>(mq, mk, mv, a, grid, s);
+    if (dk == 192 && dv == 128) return launch_t<192, 128, kBias>(mq, mk, mv, a, grid, s);
+    if (dk == 128 && dv == 64) return launch_t<128, 64, kBias>(mq, mk, mv, a, grid, s);
+    if (dk == 64 && dv == 128) return launch_t<64, 128, kBias>(mq, mk, mv, a, grid, s);
+    if (dk == 192 && dv == 64) return launch_t<192, 64, kBias>(mq, mk, mv, a, grid, s);
+    return fail(ATTN_ERR_UNSUPPORTED, "no bf16 kernel for dk=%d dv=%d", dk, dv);
+}
+
+}  // namespace
+
+attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
+    for (int t = 0; t < 3; ++t) {
+        if ((p.q_stride[t] == 0 && (t == 0 ? p.B : t == 1 ? p.Nq : p.H) > 1) ||
+            (p.Nk > 0 && ((p.k_stride[t] == 0 || p.v_stride[t] == 0) && (t == 0 ? p.B : t == 1 ? p.Nk : p.H) > 1)))
+            return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path needs non-zero q/k/v strides");
+    }
+    CUtensorMap mq, mk, mv;
+    attn_status_t st = encode(&mq, p.q, p.B, p.Nq, p.H, p.dk, p.q_stride, "q");
+    if (st) return st;
+    if (p.Nk > 0) {
+        if ((st = encode(&mk, p.k, p.B, p.Nk, p.H, p.dk, p.k_stride, "k"))) return st;
+        if ((st = encode(&mv, p.v, p.B, p.Nk, p.H, p.dv, p.v_stride, "v"))) return st;
+    } else {
+        mk = mq;  // never read: with no keys every tile is empty
+        mv = mq;
+    }
+    Args a;
+    a.B = (int)p.B; a.H = (int)p.H; a.Nq = (int)p.Nq; a.Nk = (int)p.Nk; a.causal = p.causal;
+    a.n_qt = (int)((p.Nq + BQ - 1) / BQ);
+    a.scale_log2 = p.scale * kLog2e;
+    a.o = static_cast<__nv_bfloat16 *>(p.o);
+    a.os0 = p.o_stride[0]; a.os1 = p.o_stride[1]; a.os2 = p.o_stride[2];
+    a.lse = p.lse;
+    a.bias = p.bias; a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1]; a.bs2 = p.bias_stride[2];
+    a.kv_lens = p.kv_lens;
+    a.flags = device_flags();
+    if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
+    const long long grid = (long long)a.n_qt * p.B * p.H;
+    if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
+    if (p.bias) return dispatch<true>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);
+    return dispatch<false>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);
+}
+
+}  // namespace attn

@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads and exports every entry point include/attn.h declares;
+host-side argument checks reject bad calls before any CUDA work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import online_softmax_fa2_gb300 as ofa
+from online_softmax_fa2_gb300 import build as ofa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ofa_build.build()
+    return ofa.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_decode_splitkv", "attn_merge_states",
+              "attn_decode_workspace_bytes", "attn_last_error", "attn_device_error_flags"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/attn.h but not exported"
+
+
+def test_version_and_workspace_size(lib):
+    assert lib.attn_version() >= 100
+    assert ofa.decode_workspace_bytes(64, 32, 128, 16) == 64 * 32 * 16 * 130 * 4
+    assert ofa.decode_workspace_bytes(-1, 32, 128, 16) == 0
+
+
+def _params(**kw):
+    p = ofa.Params()
+    p.dtype, p.causal = 1, 0
+    p.B, p.H, p.Nq, p.Nk, p.dk, p.dv = 1, 1, 16, 16, 128, 128
+    p.q, p.k, p.v, p.o = 0x10000, 0x20000, 0x30000, 0x40000
+    for s in ("q_stride", "k_stride", "v_stride", "o_stride"):
+        setattr(p, s, (ctypes.c_int64 * 3)(16 * 128, 128, 128))
+    p.scale = 0.088
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=7), ofa.Status.INVALID_ARG),
+    (dict(causal=2), ofa.Status.INVALID_ARG),
+    (dict(B=-1), ofa.Status.INVALID_ARG),
+    (dict(dk=0), ofa.Status.INVALID_ARG),
+    (dict(scale=float("nan")), ofa.Status.INVALID_ARG),
+    (dict(q=None), ofa.Status.INVALID_ARG),
+    (dict(dk=96, dv=96), ofa.Status.UNSUPPORTED),
+    (dict(dv=192), ofa.Status.UNSUPPORTED),
+    (dict(scale=-1.0), ofa.Status.UNSUPPORTED),
+    (dict(q=0x10002), ofa.Status.MISALIGNED),
+    (dict(k_stride=(ctypes.c_int64 * 3)(16 * 128, 132, 128)), ofa.Status.MISALIGNED),
+    (dict(block_k=16), ofa.Status.INVALID_ARG),
+    (dict(dtype=0, block_k=48), ofa.Status.INVALID_ARG),
+    (dict(dtype=0, dk=300), ofa.Status.UNSUPPORTED),
+])
+def test_fwd_rejects_bad_arguments_on_the_host(lib, kw, status):
+    p = _params(**kw)
+    st = lib.attn_fwd(ctypes.byref(p), None)
+    assert st == status, ofa.last_error()
+    assert ofa.last_error()
+
+
+def test_null_params_and_empty_problem(lib):
+    assert lib.attn_fwd(None, None) == ofa.Status.INVALID_ARG
+    p = _params(Nq=0)
+    assert lib.attn_fwd(ctypes.byref(p), None) == ofa.Status.OK  # nothing to do
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    p = _params(Nq=1)
+    ws = ctypes.c_void_p(0x50000)
+    assert lib.attn_decode_splitkv(ctypes.byref(p), 0, ws, 1 << 20, None) == ofa.Status.INVALID_ARG
+    assert lib.attn_decode_splitkv(ctypes.byref(p), 300, ws, 1 << 20, None) == ofa.Status.INVALID_ARG
+    assert lib.attn_decode_splitkv(ctypes.byref(p), 4, ws, 16, None) == ofa.Status.WORKSPACE
+    assert lib.attn_decode_splitkv(ctypes.byref(p), 4, None, 1 << 20, None) == ofa.Status.WORKSPACE
+    p2 = _params(Nq=2)
+    assert lib.attn_decode_splitkv(ctypes.byref(p2), 4, ws, 1 << 20, None) == ofa.Status.INVALID_ARG
+    p3 = _params(Nq=1, dtype=0)
+    assert lib.attn_decode_splitkv(ctypes.byref(p3), 4, ws, 1 << 20, None) == ofa.Status.UNSUPPORTED
+    p4 = _params(Nq=1, dk=128, dv=64)
+    assert lib.attn_decode_splitkv(ctypes.byref(p4), 4, ws, 1 << 20, None) == ofa.Status.UNSUPPORTED
+
+
+def test_merge_rejects_bad_arguments_on_the_host(lib):
+    st = (ctypes.c_int64 * 3)(128, 128, 128)
+    assert lib.attn_merge_states(None, 1, 1, 4, 128, 1, ctypes.c_void_p(0x1000), st, None,
+                                 None) == ofa.Status.INVALID_ARG
+    assert lib.attn_merge_states(ctypes.c_void_p(0x1000), 1, 1, 0, 128, 1, ctypes.c_void_p(0x1000),
+                                 st, None, None) == ofa.Status.INVALID_ARG
+    assert lib.attn_merge_states(ctypes.c_void_p(0x1000), 1, 1, 4, 128, 5, ctypes.c_void_p(0x1000),
+                                 st, None, None) == ofa.Status.INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 4, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ofa.attn_fwd(q, q, q)
