@@ -369,6 +369,64 @@ def run_ours(args):
     return 0
 
 
+CASES = {
+    # name: (workload factory kwargs, kind)
+    "prefill": ("causal_2k", {}, "fwd"),
+    "padbias": ("padded_bias", {}, "fwd"),
+    "long_causal": ("long_causal", {}, "fwd"),
+    "fp32": ("fp32_small", {}, "fwd"),
+    "decode": ("decode", {}, "decode"),
+    "decode_b16": ("decode", {"B": 16}, "decode"),
+}
+
+
+def run_case(args):
+    """Run one workload's kernels `--steps` times after `--warmup` (no extras): per-launch
+    device time and throughput.  Used for the other workloads and as the command under ncu."""
+    import torch
+    import online_softmax_fa2_gb300 as ofa
+    from online_softmax_fa2_gb300 import workloads as wl
+
+    fac, kw, kind = CASES[args.case]
+    dev = torch.device("cuda", 0)
+    a = getattr(wl, fac)(dev, **kw)
+    ofa.load()
+    if kind == "fwd":
+        o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
+        lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
+        fn = lambda: ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
+                                  scale=a.scale, out=o, lse=lse)
+        work, unit = a.flops() / 1e12, "TFLOP/s"
+    else:
+        ws = torch.empty(ofa.decode_workspace_bytes(a.B, a.H, a.dv, a.num_splits) // 4,
+                         dtype=torch.float32, device=dev)
+        o = torch.empty((a.B, 1, a.H, a.dv), dtype=a.q.dtype, device=dev)
+        lse = torch.empty((a.B, a.H, 1), dtype=torch.float32, device=dev)
+        fn = lambda: ofa.attn_decode_splitkv(a.q, a.k, a.v, kv_lens=a.kv_lens, bias=a.bias,
+                                             num_splits=a.num_splits, scale=a.scale,
+                                             workspace=ws, out=o, lse=lse)
+        work, unit = a.kv_bytes() / 1e9, "GB/s"
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    ms = sorted(s.elapsed_time(e) for s, e in ts)
+    med = ms[len(ms) // 2]
+    print(json.dumps({"case": args.case, "workload": a.name, "ms_median": med, "ms_min": ms[0],
+                      "value_median": work / (med / 1e3), "unit": unit, "steps": args.steps,
+                      "error_flags": ofa.device_error_flags()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,9 +436,13 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="time one workload's kernels only (also the command profiled by ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.case:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -90,8 +90,9 @@ typedef enum {
  *                       must be 0 for bfloat16
  *
  * bfloat16 path (tcgen05 tensor cores): dk in {64, 128, 192}, dv in {64, 128},
- *   scale > 0; q, k, v base pointers 16-byte aligned and their b, n, h strides multiples of
- *   8 elements (16 bytes).
+ *   scale > 0; q, k, v, o base pointers 16-byte aligned and their b, n, h strides non-zero
+ *   multiples of 8 elements (16 bytes); bias 4-byte aligned (rows that are 16-byte aligned
+ *   are read with 16-byte loads).
  * float32 path (exact fp32 SIMT): 1 <= dk, dv <= 256; any finite scale.
  */
 typedef struct {

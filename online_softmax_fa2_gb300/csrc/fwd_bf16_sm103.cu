@@ -10,8 +10,10 @@
 //   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage shared-memory ring
 //               (128-byte swizzled panels of 64 columns, the layout the tensor cores read).
 //   warp 1      tensor-core issuer (one thread): S_j = Q K_j^T into tensor memory (TMEM),
-//               double-buffered so S_{j+1} is computed while the softmax works on S_j, then
-//               O += P_j V_j with P_j read from TMEM.  Also owns the TMEM allocation.
+//               into one of three buffers so S_{j+1} is computed while the softmax works on
+//               S_j, then O += P_j V_j with P_j read from TMEM.  A buffer is reused only after
+//               the P V product that read it has completed (a tcgen05.commit per buffer), so
+//               the next S never overwrites a P still being read.  Owns the TMEM allocation.
 //   warps 4-7   softmax: thread t owns query row t (TMEM lane t), so row maxima and row sums
 //               need no shuffles.  Per key tile: load the row of S from TMEM, scale (and add
 //               the bias), mask in global positions, take the new maximum, form
@@ -59,7 +61,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units: keep the reference while x - m <= 8
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;   // O accumulator columns [256, 256 + dv); S buffers at 0, 128
+constexpr int kSBufs = 3;          // S/P buffers: TMEM columns [0,128), [128,256), [256,384)
+constexpr uint32_t kTmemO = 384;   // O accumulator columns [384, 384 + dv)
 
 struct Args {
     int B, H, Nq, Nk, causal, n_qt;
@@ -76,8 +79,9 @@ struct Args {
 struct Ctrl {
     uint64_t q_full;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], p_full[2];
-    uint64_t o_done;
+    uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
+    uint64_t o_done;     // one completion per P V product (O rescale waits on PV_{j-1})
+    uint64_t o_final;    // completes once, after the last P V product
     uint64_t final_mma;
     uint32_t tmem_base;
     int abort;
@@ -146,11 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&ctrl->v_full[s], 1);
             ptx::mbar_init(&ctrl->kv_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kSBufs; ++s) {
             ptx::mbar_init(&ctrl->s_full[s], 1);
             ptx::mbar_init(&ctrl->p_full[s], 128);
+            ptx::mbar_init(&ctrl->pv_done[s], 1);
         }
         ptx::mbar_init(&ctrl->o_done, 1);
+        ptx::mbar_init(&ctrl->o_final, 1);
         ptx::mbar_init(&ctrl->final_mma, 1);
         ctrl->abort = 0;
         ptx::fence_mbar_init();
@@ -212,7 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_addr = ptx::smem_u32(sQ);
             bool ok = ptx::mbar_wait(&ctrl->q_full, 0, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
             auto issue_s = [&](int j) -> bool {
-                const int st = j % kStages, buf = j & 1;
+                const int st = j % kStages, buf = j % kSBufs;
+                // buffer reuse: the P V product of tile j - 3 (which read this buffer) is done
+                if (j >= kSBufs &&
+                    !ptx::mbar_wait(&ctrl->pv_done[buf], ((j / kSBufs) - 1) & 1, abort, a.flags,
+                                    kFlagWaitTimeout, kWaitLimitNs))
+                    return false;
                 if (!ptx::mbar_wait(&ctrl->k_full[st], (j / kStages) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
                     return false;
@@ -230,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ok = issue_s(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-                const int st = j % kStages, buf = j & 1;
-                if (!ptx::mbar_wait(&ctrl->p_full[buf], (j >> 1) & 1, abort, a.flags, kFlagWaitTimeout,
-                                    kWaitLimitNs))
+                const int st = j % kStages, buf = j % kSBufs;
+                if (!ptx::mbar_wait(&ctrl->p_full[buf], (j / kSBufs) & 1, abort, a.flags,
+                                    kFlagWaitTimeout, kWaitLimitNs))
                     break;
                 if (!ptx::mbar_wait(&ctrl->v_full[st], (j / kStages) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
@@ -250,7 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(&ctrl->o_done);
+                ptx::mma_commit(&ctrl->pv_done[buf]);
                 ptx::mma_commit(&ctrl->kv_empty[st]);
+                if (j == n_tiles - 1) ptx::mma_commit(&ctrl->o_final);
             }
             // all tensor-core work of this CTA done before TMEM is released
             ptx::mma_commit(&ctrl->final_mma);
@@ -262,8 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = q0 + r;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
         const float c = a.scale_log2;
-        const float* bias_row = nullptr;
+        const float *bias_row = nullptr;
         if (kBias && i < a.Nq) bias_row = a.bias + b * a.bs0 + h * a.bs1 + (long long)i * a.bs2;
+        const bool bias_vec = (reinterpret_cast<uintptr_t>(bias_row) & 15u) == 0;  // float4 loads
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         // every lane waits; the warp goes on only if all lanes succeeded (tcgen05.ld/st and
@@ -274,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         for (int j = 0; j < n_tiles; ++j) {
-            const int buf = j & 1, kv0 = j * BK;
-            if (!wait_warp(&ctrl->s_full[buf], (j >> 1) & 1)) {
+            const int buf = j % kSBufs, kv0 = j * BK;
+            if (!wait_warp(&ctrl->s_full[buf], (j / kSBufs) & 1)) {
                 ok = false;
                 break;
             }
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k4 = 0; k4 < BK / 4; ++k4) {
                     float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
                     const int key = kv0 + 4 * k4;
-                    if (bias_row && key + 3 < n)
+                    if (bias_row && bias_vec && key + 3 < n)
                         bb = __ldg(reinterpret_cast<const float4 *>(bias_row + key));
                     else if (bias_row) {
                         float t[4] = {0.f, 0.f, 0.f, 0.f};
@@ -348,7 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l_run = fmaf(alpha, l_run, lsum);
 
-            // u <- alpha * u: rescale this warp's O rows once PV_{j-1} has landed
+            // u <- alpha * u: rescale this warp's O rows once PV_{j-1} has landed.  (The
+            // commit behind s_full for S_j covers PV_{j-2}, so o_done is in phase j-1 or j
+            // here and its parity is unambiguous.)
             if (__any_sync(0xffffffffu, rescale)) {
                 if (!wait_warp(&ctrl->o_done, (j - 1) & 1)) {
                     ok = false;
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf
-        if (ok && wait_warp(&ctrl->o_done, (n_tiles - 1) & 1)) {
+        if (ok && wait_warp(&ctrl->o_final, 0)) {
             ptx::tc_fence_after();
             const bool empty = !(l_run > 0.f);
             const float inv = empty ? 0.f : 1.f / l_run;
