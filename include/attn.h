@@ -150,6 +150,25 @@ attn_status_t attn_decode_splitkv(const attn_fwd_params_t *params, int32_t num_s
                                   attn_stream_t stream);
 
 /*
+ * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot allocate device
+ * memory when they decode (a framework whose allocator owns the device memory, a plugin
+ * handed only its inputs and outputs, a latency-bound loop where cudaMalloc would
+ * synchronise the device).  The paper has no counterpart: the pages describe no such variant.
+ *   - Same arguments, checks, kernels and results as attn_decode_splitkv, without the
+ *     workspace: the partial states go to a device array built into the library, 32 MiB
+ *     (B * H * num_splits * (2 + dv) * 4 bytes must fit; larger problems return
+ *     ATTN_ERR_WORKSPACE and queue nothing).  Every device that loads the library holds that
+ *     array until the process exits.  No device memory is allocated by any call.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - All calls share the one array.  Every call writes each partial state it reads, so
+ *     nothing needs clearing, but calls whose work overlaps on the GPU (different streams,
+ *     several host threads) race on it: order them on one stream.
+ */
+attn_status_t attn_decode_splitkv_noalloc(const attn_fwd_params_t *params, int32_t num_splits,
+                                          attn_stream_t stream);
+
+/*
  * attn_merge_states -- merge S partial states per (b, h) and finalise.
  * ("How Does FlashAttention Preserve Global Softmax Across Tiles?", section 3: put both
  *  maxima into the common maximum, scale l and u of each part by exp(m_s - m), add;

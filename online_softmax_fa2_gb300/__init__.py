@@ -23,7 +23,8 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "attn_decode_splitkv", "attn_merge_states", "decode_workspace_bytes",
+__all__ = ["attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc", "attn_merge_states",
+           "decode_workspace_bytes",
            "device_error_flags", "last_error", "library_path", "load", "AttnError", "Status"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,6 +91,8 @@ def load():
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_splitkv.argtypes = [P, i32, vp, ctypes.c_size_t, vp]
         lib.attn_decode_splitkv.restype = i32
+        lib.attn_decode_splitkv_noalloc.argtypes = [P, i32, vp]
+        lib.attn_decode_splitkv_noalloc.restype = i32
         lib.attn_merge_states.argtypes = [vp, i64, i64, i32, i64, i32, vp,
                                           ctypes.POINTER(ctypes.c_int64), vp, vp]
         lib.attn_merge_states.restype = i32
@@ -225,6 +228,25 @@ def attn_decode_splitkv(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=N
     _check(lib.attn_decode_splitkv(ctypes.byref(p), int(num_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse, workspace
+
+
+def attn_decode_splitkv_noalloc(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=None,
+                                out=None, lse=None, stream=None):
+    """Split-KV decode that allocates no device memory in the library: for callers that
+    cannot allocate while decoding.  The partial states go to a 32 MiB device array built
+    into the library (shared by every call: order calls on one stream).  The first call on a
+    device looks up that array's address; make it before any stream capture.  Returns
+    (o, lse); o and lse are allocated here only when not passed in."""
+    lib = load()
+    B, Nq, H, _ = q.shape
+    dv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, Nq, H, dv), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    p = make_params(q, k, v, out, lse, bias, kv_lens, False, scale, 0)
+    _check(lib.attn_decode_splitkv_noalloc(ctypes.byref(p), int(num_splits), _stream(stream)))
+    return out, lse
 
 
 def attn_merge_states(partials, out_dtype=torch.bfloat16, out=None, lse=None, stream=None):

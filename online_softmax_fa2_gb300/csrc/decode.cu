@@ -16,6 +16,7 @@
 // gives each exponential.  The G group states are then merged in shared memory and the
 // split's state is written in natural-log units.
 #include <cmath>
+#include <mutex>
 
 #include <cuda_bf16.h>
 
@@ -265,3 +266,64 @@ attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int num_
 }
 
 }  // namespace attn
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// Some callers cannot allocate device memory at the moment they decode: a host framework
+// whose caching allocator already owns the device memory and forbids side allocations, a
+// plugin that is handed only its input and output buffers, or a latency-bound serving loop
+// in which cudaMalloc/cudaFree would synchronise the device.  For them the split kernel's
+// partial states live in one statically allocated device array of this file, sized for up to
+// kNoAllocScratchBytes; every device that loads the library holds this array until the
+// process exits.  The kernels, the arguments checks and the results are those of
+// attn_decode_splitkv: this entry point only supplies the workspace.
+namespace attn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 32u << 20;  // 32 MiB of partial states
+
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// Host code cannot use g_decode_scratch's name as a device address, so the address is looked
+// up once per device (with that device current) and cached.
+void *g_scratch_addr[64];
+std::mutex g_scratch_mutex;
+
+attn_status_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(ATTN_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+        if (e != cudaSuccess)
+            return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status_t attn_decode_splitkv_noalloc(const attn_fwd_params_t *p, int32_t num_splits,
+                                                     attn_stream_t stream) {
+    using namespace attn;
+    if (p && num_splits >= 1) {
+        const size_t need = attn_decode_workspace_bytes(p->B, p->H, p->dv, num_splits);
+        if (need > kNoAllocScratchBytes)
+            return fail(ATTN_ERR_WORKSPACE,
+                        "allocation-free decode needs %zu bytes of partial states for B=%lld H=%lld "
+                        "dv=%lld num_splits=%d; its built-in scratch holds %zu",
+                        need, (long long)p->B, (long long)p->H, (long long)p->dv, num_splits,
+                        kNoAllocScratchBytes);
+    }
+    void *scratch = nullptr;
+    attn_status_t st = noalloc_scratch(&scratch);
+    if (st) return st;
+    return attn_decode_splitkv(p, num_splits, scratch, kNoAllocScratchBytes, stream);
+}
