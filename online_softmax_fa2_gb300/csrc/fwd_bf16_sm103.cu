@@ -7,8 +7,10 @@
 // the hardware hands them to SMs as SMs free up.
 //
 // Roles (256 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage shared-memory ring
+//   warp 0      TMA producer: Q once, then K and V tiles into two shared-memory rings
 //               (128-byte swizzled panels of 64 columns, the layout the tensor cores read).
+//               A K slot is released as soon as S = Q K^T has read it and a V slot when
+//               O += P V has, so loads run several tiles ahead of the tensor cores.
 //   warp 1      tensor-core issuer (one thread): S_j = Q K_j^T into tensor memory (TMEM),
 //               into one of three buffers so S_{j+1} is computed while the softmax works on
 //               S_j, then O += P_j V_j with P_j read from TMEM.  A buffer is reused only after
@@ -53,7 +55,6 @@ namespace {
 
 constexpr int BQ = 128;            // query rows per tile (= MMA M = TMEM lanes)
 constexpr int BK = 128;            // keys per tile (= N of S = Q K^T, = K of O += P V)
-constexpr int kStages = 2;         // K/V shared-memory ring depth
 constexpr int kThreads = 256;
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes), 128B-swizzled
 constexpr float kLog2e = 1.4426950408889634f;
@@ -76,9 +77,11 @@ struct Args {
     uint32_t *flags;
 };
 
+constexpr int kMaxStages = 4;
+
 struct Ctrl {
     uint64_t q_full;
-    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
     uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
     uint64_t o_done;     // one completion per P V product (O rescale waits on PV_{j-1})
     uint64_t o_final;    // completes once, after the last P V product
@@ -92,9 +95,16 @@ struct Layout {
     static constexpr int kQBytes = (DK / 64) * kPanelBytes;
     static constexpr int kKBytes = (DK / 64) * kPanelBytes;
     static constexpr int kVBytes = (DV / 64) * kPanelBytes;
-    static constexpr int kStageBytes = kKBytes + kVBytes;
-    static constexpr int kDataBytes = kQBytes + kStages * kStageBytes;
+    static constexpr int kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
+    // deepest equal K and V rings that fit next to Q
+    static constexpr int kStages =
+        (kQBytes + 4 * (kKBytes + kVBytes) + 2048 <= kSmemMax) ? 4
+        : (kQBytes + 3 * (kKBytes + kVBytes) + 2048 <= kSmemMax) ? 3 : 2;
+    static constexpr int kKOff = kQBytes;                       // K ring
+    static constexpr int kVOff = kQBytes + kStages * kKBytes;   // V ring
+    static constexpr int kDataBytes = kVOff + kStages * kVBytes;
     static constexpr int kBytes = kDataBytes + (int)sizeof(Ctrl) + 1024;  // + alignment slack
+    static_assert(kBytes <= kSmemMax, "shared memory budget");
 };
 
 __device__ __forceinline__ float max4(float a, float b, float c, float d) {
@@ -106,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Args a) {
     using L = Layout<DK, DV>;
+    constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -147,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&ctrl->q_full, 1);
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&ctrl->k_full[s], 1);
+            ptx::mbar_init(&ctrl->k_empty[s], 1);
             ptx::mbar_init(&ctrl->v_full[s], 1);
-            ptx::mbar_init(&ctrl->kv_empty[s], 1);
+            ptx::mbar_init(&ctrl->v_empty[s], 1);
         }
         for (int s = 0; s < kSBufs; ++s) {
             ptx::mbar_init(&ctrl->s_full[s], 1);
@@ -182,32 +194,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int p = 0; p < DK / 64; ++p)
                 ptx::tma_load_4d(sQ + p * kPanelBytes, &tm_q, &ctrl->q_full, p * 64, q0, h, b);
-            int last_issued = -1;
+            int last_k = -1, last_v = -1;  // last tiles whose K / V copies were issued
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kStages;
                 if (j >= kStages &&
-                    !ptx::mbar_wait(&ctrl->kv_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
+                    !ptx::mbar_wait(&ctrl->k_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
                     break;
-                uint8_t *sK = smem + L::kQBytes + st * L::kStageBytes;
-                uint8_t *sV = sK + L::kKBytes;
+                uint8_t *sK = smem + L::kKOff + st * L::kKBytes;
+                uint8_t *sV = smem + L::kVOff + st * L::kVBytes;
                 ptx::mbar_arrive_expect_tx(&ctrl->k_full[st], L::kKBytes);
 #pragma unroll
                 for (int p = 0; p < DK / 64; ++p)
                     ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[st], p * 64, j * BK, h, b);
+                last_k = j;
+                if (j >= kStages &&
+                    !ptx::mbar_wait(&ctrl->v_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
+                                    kFlagWaitTimeout, kWaitLimitNs))
+                    break;
                 ptx::mbar_arrive_expect_tx(&ctrl->v_full[st], L::kVBytes);
 #pragma unroll
                 for (int p = 0; p < DV / 64; ++p)
                     ptx::tma_load_4d(sV + p * kPanelBytes, &tm_v, &ctrl->v_full[st], p * 64, j * BK, h, b);
-                last_issued = j;
+                last_v = j;
             }
             if (*abort) {  // let copies still in flight land before the CTA exits
                 ptx::mbar_wait_quiet(&ctrl->q_full, 0, kWaitLimitNs);
-                for (int j = max(0, last_issued - kStages + 1); j <= last_issued; ++j) {
-                    const int st = j % kStages;
-                    ptx::mbar_wait_quiet(&ctrl->k_full[st], (j / kStages) & 1, kWaitLimitNs);
-                    ptx::mbar_wait_quiet(&ctrl->v_full[st], (j / kStages) & 1, kWaitLimitNs);
-                }
+                for (int j = max(0, last_k - kStages + 1); j <= last_k; ++j)
+                    ptx::mbar_wait_quiet(&ctrl->k_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
+                for (int j = max(0, last_v - kStages + 1); j <= last_v; ++j)
+                    ptx::mbar_wait_quiet(&ctrl->v_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
@@ -228,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     kFlagWaitTimeout, kWaitLimitNs))
                     return false;
                 ptx::tc_fence_after();
-                const uint32_t k_addr = ptx::smem_u32(smem + L::kQBytes + st * L::kStageBytes);
+                const uint32_t k_addr = ptx::smem_u32(smem + L::kKOff + st * L::kKBytes);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = (kk / 4) * kPanelBytes + (kk % 4) * 32;
@@ -236,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ptx::sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(&ctrl->s_full[buf]);
+                ptx::mma_commit(&ctrl->k_empty[st]);
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -249,8 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     kFlagWaitTimeout, kWaitLimitNs))
                     break;
                 ptx::tc_fence_after();
-                const uint32_t v_addr =
-                    ptx::smem_u32(smem + L::kQBytes + st * L::kStageBytes + L::kKBytes);
+                const uint32_t v_addr = ptx::smem_u32(smem + L::kVOff + st * L::kVBytes);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // P: bf16 pairs packed in TMEM columns (8 columns per 16 keys);
@@ -262,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::mma_commit(&ctrl->o_done);
                 ptx::mma_commit(&ctrl->pv_done[buf]);
-                ptx::mma_commit(&ctrl->kv_empty[st]);
+                ptx::mma_commit(&ctrl->v_empty[st]);
                 if (j == n_tiles - 1) ptx::mma_commit(&ctrl->o_final);
             }
             // all tensor-core work of this CTA done before TMEM is released
@@ -308,8 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < BK; ++k) x[k] = __uint_as_float(raw[k]);
             }
-            // logits in base-2 units; masked ones become -inf
+            // Logits in base-2 units are x = S * c (+ bias * log2 e); masked ones are -inf.
+            // Without a bias the scale is folded into the exponent (p = 2^(S*c - m), one FFMA
+            // per element) and the row maximum is taken on raw S (c > 0).  Max and sum use 8
+            // independent partial results to keep the dependency chains short.
             const bool need_mask = (kv0 + BK > n) || (a.causal && kv0 + BK - 1 > q0 + shift);
+            const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim visible
             if (kBias) {
 #pragma unroll
                 for (int k4 = 0; k4 < BK / 4; ++k4) {
@@ -328,19 +348,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x[4 * k4 + 2] = fmaf(x[4 * k4 + 2], c, bb.z * kLog2e);
                     x[4 * k4 + 3] = fmaf(x[4 * k4 + 3], c, bb.w * kLog2e);
                 }
-            } else {
-#pragma unroll
-                for (int k = 0; k < BK; ++k) x[k] *= c;
             }
             if (need_mask) {
-                const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim visible
 #pragma unroll
                 for (int k = 0; k < BK; ++k)
                     if (kv0 + k >= lim) x[k] = -INFINITY;
             }
-            float mt = -INFINITY;
+            float mt;
+            {
+                float m8[8];
 #pragma unroll
-            for (int k = 0; k < BK; k += 4) mt = fmaxf(mt, max4(x[k], x[k + 1], x[k + 2], x[k + 3]));
+                for (int t = 0; t < 8; ++t) m8[t] = x[t];
+#pragma unroll
+                for (int k = 8; k < BK; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
+                mt = max4(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]), fmaxf(m8[4], m8[5]),
+                          fmaxf(m8[6], m8[7]));
+                if (!kBias) mt *= c;  // raw maximum -> base-2 units
+            }
 
             float alpha = 1.f;
             bool rescale = false;
@@ -354,11 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-            float lsum = 0.f;
+            float lsum;
+            {
+                float s8[8];
 #pragma unroll
-            for (int k = 0; k < BK; ++k) {
-                x[k] = ptx::ex2(x[k] - mref);
-                lsum += x[k];
+                for (int t = 0; t < 8; ++t) s8[t] = 0.f;
+#pragma unroll
+                for (int k = 0; k < BK; ++k) {
+                    x[k] = kBias ? ptx::ex2(x[k] - mref) : ptx::ex2(fmaf(x[k], c, -mref));
+                    s8[k & 7] += x[k];
+                }
+                lsum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
             }
             l_run = fmaf(alpha, l_run, lsum);
 
@@ -393,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int row = r;  // one key row per thread
                 if (kv0 + row >= n && kv0 + row < a.Nk) {
-                    uint8_t *sV = smem + L::kQBytes + st * L::kStageBytes + L::kKBytes;
+                    uint8_t *sV = smem + L::kVOff + st * L::kVBytes;
 #pragma unroll
                     for (int p = 0; p < DV / 64; ++p) {
                         uint4 *dst = reinterpret_cast<uint4 *>(sV + p * kPanelBytes + row * 128);
