@@ -1,0 +1,239 @@
+// fwd_bf16_common.cuh -- pieces shared by the two bf16 prefill kernels (one 128-row query tile
+// per CTA, and two tiles per CTA): arguments, tile constants, and the per-row softmax steps
+// that run on one thread per query row (the row's TMEM lane).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "attn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace bf16fwd {
+
+constexpr int BQ = 128;                 // query rows per tile (= MMA M = TMEM lanes)
+constexpr int BK = 128;                 // keys per tile (= N of S = Q K^T, = K of O += P V)
+constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes), 128B-swizzled
+constexpr int kSmemMax = 232448;        // 227 KB of dynamic shared memory per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// A row keeps its reference maximum until a tile's maximum exceeds it by more than 8 in
+// base-2 units (a factor 256): rescaling is exact for any reference shared by l and u, and
+// exponentials <= 256 stay far from fp32/bf16 overflow.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // every mbarrier wait gives up after 1 s
+
+struct Args {
+    int B, H, Nq, Nk, causal, n_items;
+    float scale_log2;
+    __nv_bfloat16 *o;
+    long long os0, os1, os2;
+    float *lse;
+    const float *bias;
+    long long bs0, bs1, bs2;
+    const int *kv_lens;
+    uint32_t *flags;
+};
+
+// Key length of sequence b, clamped to [0, Nk] (a clamp is reported once per sequence).
+__device__ __forceinline__ int seq_len(const Args &a, int b, bool report) {
+    if (!a.kv_lens) return a.Nk;
+    const int raw = a.kv_lens[b];
+    const int n = min(max(raw, 0), a.Nk);
+    if (raw != n && report) atomicOr(a.flags, kFlagKvLenClamped);
+    return n;
+}
+
+// Number of 128-key tiles a query tile starting at row r0 must visit: keys past the last
+// visible key of its last row are never loaded (causal: key j visible to row i iff
+// j <= i + n - Nq, i.e. the sequences' ends aligned).
+__device__ __forceinline__ int kv_tiles(const Args &a, int r0, int n) {
+    if (r0 >= a.Nq) return 0;
+    int kv_end = n;
+    if (a.causal) kv_end = min(n, max(0, min(r0 + BQ, a.Nq) + n - a.Nq));
+    return (kv_end + BK - 1) / BK;
+}
+
+// The row of S held in TMEM columns [col, col + BK) of this thread's lane.
+__device__ __forceinline__ void load_s_row(uint32_t taddr, float (&x)[BK]) {
+    uint32_t raw[BK];
+#pragma unroll
+    for (int cc = 0; cc < BK / 32; ++cc)
+        ptx::tmem_ld32(taddr + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[cc * 32]));
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int cc = 0; cc < BK / 32; ++cc)
+        ptx::reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&raw[cc * 32]));
+#pragma unroll
+    for (int k = 0; k < BK; ++k) x[k] = __uint_as_float(raw[k]);
+}
+
+// Turns a row of S into what the maximum is taken on and returns the tile maximum in base-2
+// units (-inf when no key of the tile is visible).  With a bias, x becomes the base-2 logit
+// S*c + b*log2(e); without one, x stays raw S and the scale is applied to the maximum only
+// (c > 0) and later inside the exponent.  Keys >= lim become -inf (a select: whatever is
+// stored at a masked position, NaN included, is dropped here).
+template <bool kBias>
+__device__ __forceinline__ float tile_logits(float (&x)[BK], float c, const float *bias_row,
+                                             bool bias_vec, int kv0, int n, bool need_mask,
+                                             int lim) {
+    if (kBias) {
+#pragma unroll
+        for (int k4 = 0; k4 < BK / 4; ++k4) {
+            float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int key = kv0 + 4 * k4;
+            if (bias_row && bias_vec && key + 3 < n)
+                bb = __ldg(reinterpret_cast<const float4 *>(bias_row + key));
+            else if (bias_row) {
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int e = 0; e < 4; ++e)
+                    if (key + e < n) t[e] = bias_row[key + e];
+                bb = make_float4(t[0], t[1], t[2], t[3]);
+            }
+            x[4 * k4 + 0] = fmaf(x[4 * k4 + 0], c, bb.x * kLog2e);
+            x[4 * k4 + 1] = fmaf(x[4 * k4 + 1], c, bb.y * kLog2e);
+            x[4 * k4 + 2] = fmaf(x[4 * k4 + 2], c, bb.z * kLog2e);
+            x[4 * k4 + 3] = fmaf(x[4 * k4 + 3], c, bb.w * kLog2e);
+        }
+    }
+    if (need_mask) {
+#pragma unroll
+        for (int k = 0; k < BK; ++k)
+            if (kv0 + k >= lim) x[k] = -INFINITY;
+    }
+    float m8[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) m8[t] = x[t];
+#pragma unroll
+    for (int k = 8; k < BK; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
+    float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    if (!kBias) mt *= c;
+    return mt;
+}
+
+// New reference maximum for a row ("choose the new maximum"): the first visible key sets it
+// (the old state has no mass, so nothing is rescaled); afterwards it moves only when the tile
+// maximum exceeds it by more than kRescaleThreshold, and then alpha = 2^(m_old - m_new).
+__device__ __forceinline__ float update_max(float mt, float &m_run, bool &rescale) {
+    rescale = false;
+    if (mt == -INFINITY) return 1.f;
+    if (m_run == -INFINITY) {
+        m_run = mt;
+        return 1.f;
+    }
+    if (mt > m_run + kRescaleThreshold) {
+        const float alpha = ptx::ex2(m_run - mt);
+        m_run = mt;
+        rescale = true;
+        return alpha;
+    }
+    return 1.f;
+}
+
+// p = 2^(x - m) in place (one FFMA + one ex2 per element); returns the row's tile mass.
+template <bool kBias>
+__device__ __forceinline__ float tile_exp(float (&x)[BK], float c, float m_run) {
+    const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+    float s8[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) s8[t] = 0.f;
+#pragma unroll
+    for (int k = 0; k < BK; ++k) {
+        x[k] = kBias ? ptx::ex2(x[k] - mref) : ptx::ex2(fmaf(x[k], c, -mref));
+        s8[k & 7] += x[k];
+    }
+    return ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+}
+
+// P rounded to bf16, packed two per 32-bit TMEM column (lower key in the low half), into the
+// columns [taddr, taddr + BK/2) that held S.
+__device__ __forceinline__ void store_p(uint32_t taddr, const float (&x)[BK]) {
+#pragma unroll
+    for (int cc = 0; cc < BK / 64; ++cc) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) pk[t] = ptx::pack_bf16x2(x[cc * 64 + 2 * t], x[cc * 64 + 2 * t + 1]);
+        ptx::tmem_st32(taddr + cc * 32, pk);
+    }
+    ptx::tmem_st_wait();
+}
+
+// u <- alpha * u for this lane's DV accumulator columns at taddr.
+template <int DV>
+__device__ __forceinline__ void scale_o(uint32_t taddr, float alpha) {
+#pragma unroll
+    for (int cc = 0; cc < DV / 32; ++cc) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(taddr + cc * 32, ov);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(ov);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+        ptx::tmem_st32(taddr + cc * 32, ov);
+    }
+    ptx::tmem_st_wait();
+}
+
+// Divide once: o = u / l rounded to bf16 into orow (skipped when orow is null: a row past Nq),
+// lse = (m + log2 l) * ln 2.  An empty row (l == 0) gives +0.0 and -inf.  Warp-collective.
+template <int DV>
+__device__ __forceinline__ void write_row(uint32_t taddr, float l_run, float m_run,
+                                          __nv_bfloat16 *orow, float *lse_out) {
+    const bool empty = !(l_run > 0.f);
+    const float inv = empty ? 0.f : 1.f / l_run;
+    uint4 *o4 = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+    for (int cc = 0; cc < DV / 32; ++cc) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(taddr + cc * 32, ov);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            pk[t] = empty ? 0u
+                          : ptx::pack_bf16x2(__uint_as_float(ov[2 * t]) * inv,
+                                             __uint_as_float(ov[2 * t + 1]) * inv);
+        if (o4) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                o4[cc * 4 + t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+    }
+    if (lse_out) *lse_out = empty ? -INFINITY : (m_run + log2f(l_run)) * kLn2;
+}
+
+// A row that sees no key at all: o = +0.0, lse = -inf (no TMEM involved).
+template <int DV>
+__device__ __forceinline__ void write_empty_row(__nv_bfloat16 *orow, float *lse_out) {
+    uint4 *o4 = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+    for (int c = 0; c < DV / 8; ++c) o4[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (lse_out) *lse_out = -INFINITY;
+}
+
+// Zero value row `row` (all DV columns) of a V tile in shared memory.  In the 128-byte
+// swizzled layout a row's 16-byte chunks are permuted only within that row's 128 bytes, so
+// clearing the row's bytes in every 64-column panel clears exactly that key.
+template <int DV>
+__device__ __forceinline__ void zero_v_row(uint8_t *sV, int row) {
+#pragma unroll
+    for (int p = 0; p < DV / 64; ++p) {
+        uint4 *dst = reinterpret_cast<uint4 *>(sV + p * kPanelBytes + row * 128);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) dst[t] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+}  // namespace bf16fwd
+
+// Launches the two-tile kernel (dk <= 128); defined in fwd_bf16_pair_sm103.cu.
+attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
+                                   const CUtensorMap &mv, const bf16fwd::Args &a, int dk, int dv,
+                                   bool bias, cudaStream_t s);
+
+}  // namespace attn

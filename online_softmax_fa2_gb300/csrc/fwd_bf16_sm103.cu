@@ -40,43 +40,21 @@
 // Every mbarrier wait is bounded (1 s of wall time): on expiry the thread raises a CTA-wide
 // abort flag and the device error word, every role leaves its loop, in-flight copies and
 // tensor-core work are waited for (again bounded), TMEM is freed and the CTA exits.
-#include <cuda.h>
-#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
-#include <cmath>
 #include <mutex>
 
-#include "attn_internal.h"
-#include "sm100_ptx.cuh"
+#include "fwd_bf16_common.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int BQ = 128;            // query rows per tile (= MMA M = TMEM lanes)
-constexpr int BK = 128;            // keys per tile (= N of S = Q K^T, = K of O += P V)
+using namespace bf16fwd;
+
 constexpr int kThreads = 256;
-constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes), 128B-swizzled
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // base-2 units: keep the reference while x - m <= 8
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;          // S/P buffers: TMEM columns [0,128), [128,256), [256,384)
 constexpr uint32_t kTmemO = 384;   // O accumulator columns [384, 384 + dv)
-
-struct Args {
-    int B, H, Nq, Nk, causal, n_qt;
-    float scale_log2;
-    __nv_bfloat16 *o;
-    long long os0, os1, os2;
-    float *lse;
-    const float *bias;
-    long long bs0, bs1, bs2;
-    const int *kv_lens;
-    uint32_t *flags;
-};
-
 constexpr int kMaxStages = 4;
 
 struct Ctrl {
@@ -95,7 +73,6 @@ struct Layout {
     static constexpr int kQBytes = (DK / 64) * kPanelBytes;
     static constexpr int kKBytes = (DK / 64) * kPanelBytes;
     static constexpr int kVBytes = (DV / 64) * kPanelBytes;
-    static constexpr int kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
     // deepest equal K and V rings that fit next to Q
     static constexpr int kStages =
         (kQBytes + 4 * (kKBytes + kVBytes) + 2048 <= kSmemMax) ? 4
@@ -106,10 +83,6 @@ struct Layout {
     static constexpr int kBytes = kDataBytes + (int)sizeof(Ctrl) + 1024;  // + alignment slack
     static_assert(kBytes <= kSmemMax, "shared memory budget");
 };
-
-__device__ __forceinline__ float max4(float a, float b, float c, float d) {
-    return fmaxf(fmaxf(a, b), fmaxf(c, d));
-}
 
 template <int DK, int DV, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -126,30 +99,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bhn = a.B * a.H;
-    const int qt = a.n_qt - 1 - (int)(blockIdx.x / bhn);  // longest first
+    const int qt = a.n_items - 1 - (int)(blockIdx.x / bhn);  // longest first
     const int bh = (int)(blockIdx.x % bhn), b = bh / a.H, h = bh % a.H;
     const int q0 = qt * BQ;
 
-    int n = a.Nk;
-    if (a.kv_lens) {
-        const int raw = a.kv_lens[b];
-        n = min(max(raw, 0), a.Nk);
-        if (raw != n && threadIdx.x == 0 && qt == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
-    }
+    const int n = seq_len(a, b, threadIdx.x == 0 && qt == 0 && h == 0);
     const int shift = n - a.Nq;  // causal: key j visible to row i iff j <= i + shift
-    int kv_end = n;
-    if (a.causal) kv_end = min(n, max(0, min(q0 + BQ, a.Nq) + shift));
-    const int n_tiles = (kv_end + BK - 1) / BK;
+    const int n_tiles = kv_tiles(a, q0, n);
 
     if (n_tiles == 0) {  // every row of this tile is empty: o = +0.0, lse = -inf
         if (warp >= 4) {
             const int i = q0 + (int)threadIdx.x - 128;
-            if (i < a.Nq) {
-                uint4 *orow = reinterpret_cast<uint4 *>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2);
-#pragma unroll
-                for (int c = 0; c < DV / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-                if (a.lse) a.lse[((long long)b * a.H + h) * a.Nq + i] = -INFINITY;
-            }
+            if (i < a.Nq)
+                write_empty_row<DV>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2,
+                                    a.lse ? a.lse + ((long long)b * a.H + h) * a.Nq + i : nullptr);
         }
         return;
     }
@@ -311,85 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_after();
             float x[BK];
-            {
-                uint32_t raw[BK];
-#pragma unroll
-                for (int cc = 0; cc < BK / 32; ++cc)
-                    ptx::tmem_ld32(lane_addr + buf * BK + cc * 32,
-                                   *reinterpret_cast<uint32_t(*)[32]>(&raw[cc * 32]));
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int cc = 0; cc < BK / 32; ++cc)
-                    ptx::reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&raw[cc * 32]));
-#pragma unroll
-                for (int k = 0; k < BK; ++k) x[k] = __uint_as_float(raw[k]);
-            }
-            // Logits in base-2 units are x = S * c (+ bias * log2 e); masked ones are -inf.
-            // Without a bias the scale is folded into the exponent (p = 2^(S*c - m), one FFMA
-            // per element) and the row maximum is taken on raw S (c > 0).  Max and sum use 8
-            // independent partial results to keep the dependency chains short.
+            load_s_row(lane_addr + buf * BK, x);
             const bool need_mask = (kv0 + BK > n) || (a.causal && kv0 + BK - 1 > q0 + shift);
             const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim visible
-            if (kBias) {
-#pragma unroll
-                for (int k4 = 0; k4 < BK / 4; ++k4) {
-                    float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int key = kv0 + 4 * k4;
-                    if (bias_row && bias_vec && key + 3 < n)
-                        bb = __ldg(reinterpret_cast<const float4 *>(bias_row + key));
-                    else if (bias_row) {
-                        float t[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int e = 0; e < 4; ++e)
-                            if (key + e < n) t[e] = bias_row[key + e];
-                        bb = make_float4(t[0], t[1], t[2], t[3]);
-                    }
-                    x[4 * k4 + 0] = fmaf(x[4 * k4 + 0], c, bb.x * kLog2e);
-                    x[4 * k4 + 1] = fmaf(x[4 * k4 + 1], c, bb.y * kLog2e);
-                    x[4 * k4 + 2] = fmaf(x[4 * k4 + 2], c, bb.z * kLog2e);
-                    x[4 * k4 + 3] = fmaf(x[4 * k4 + 3], c, bb.w * kLog2e);
-                }
-            }
-            if (need_mask) {
-#pragma unroll
-                for (int k = 0; k < BK; ++k)
-                    if (kv0 + k >= lim) x[k] = -INFINITY;
-            }
-            float mt;
-            {
-                float m8[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) m8[t] = x[t];
-#pragma unroll
-                for (int k = 8; k < BK; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
-                mt = max4(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]), fmaxf(m8[4], m8[5]),
-                          fmaxf(m8[6], m8[7]));
-                if (!kBias) mt *= c;  // raw maximum -> base-2 units
-            }
-
-            float alpha = 1.f;
-            bool rescale = false;
-            if (mt != -INFINITY) {
-                if (m_run == -INFINITY) {
-                    m_run = mt;  // first visible key: the old state has no mass
-                } else if (mt > m_run + kRescaleThreshold) {
-                    alpha = ptx::ex2(m_run - mt);
-                    m_run = mt;
-                    rescale = true;
-                }
-            }
-            const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-            float lsum;
-            {
-                float s8[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) s8[t] = 0.f;
-#pragma unroll
-                for (int k = 0; k < BK; ++k) {
-                    x[k] = kBias ? ptx::ex2(x[k] - mref) : ptx::ex2(fmaf(x[k], c, -mref));
-                    s8[k & 7] += x[k];
-                }
-                lsum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-            }
+            const float mt = tile_logits<kBias>(x, c, bias_row, bias_vec, kv0, n, need_mask, lim);
+            bool rescale;
+            const float alpha = update_max(mt, m_run, rescale);
+            const float lsum = tile_exp<kBias>(x, c, m_run);
             l_run = fmaf(alpha, l_run, lsum);
 
             // u <- alpha * u: rescale this warp's O rows once PV_{j-1} has landed.  (The
@@ -401,17 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < DV / 32; ++cc) {
-                    uint32_t ov[32];
-                    ptx::tmem_ld32(lane_addr + kTmemO + cc * 32, ov);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence(ov);
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
-                    ptx::tmem_st32(lane_addr + kTmemO + cc * 32, ov);
-                }
-                ptx::tmem_st_wait();
+                scale_o<DV>(lane_addr + kTmemO, alpha);
             }
 
             // value rows past n inside this tile (still in bounds) may hold anything: zero them
@@ -421,28 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int row = r;  // one key row per thread
-                if (kv0 + row >= n && kv0 + row < a.Nk) {
-                    uint8_t *sV = smem + L::kVOff + st * L::kVBytes;
-#pragma unroll
-                    for (int p = 0; p < DV / 64; ++p) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(sV + p * kPanelBytes + row * 128);
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) dst[t] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
+                if (kv0 + r >= n && kv0 + r < a.Nk) zero_v_row<DV>(smem + L::kVOff + st * L::kVBytes, r);
                 ptx::fence_proxy_async_smem();
             }
 
             // P (bf16) into the TMEM columns that held S_j
-#pragma unroll
-            for (int cc = 0; cc < BK / 64; ++cc) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int t = 0; t < 32; ++t) pk[t] = ptx::pack_bf16x2(x[cc * 64 + 2 * t], x[cc * 64 + 2 * t + 1]);
-                ptx::tmem_st32(lane_addr + buf * BK + cc * 32, pk);
-            }
-            ptx::tmem_st_wait();
+            store_p(lane_addr + buf * BK, x);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&ctrl->p_full[buf]);
         }
@@ -450,31 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf
         if (ok && wait_warp(&ctrl->o_final, 0)) {
             ptx::tc_fence_after();
-            const bool empty = !(l_run > 0.f);
-            const float inv = empty ? 0.f : 1.f / l_run;
-            uint4 *orow = (i < a.Nq)
-                              ? reinterpret_cast<uint4 *>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2)
-                              : nullptr;
-#pragma unroll
-            for (int cc = 0; cc < DV / 32; ++cc) {
-                uint32_t ov[32];
-                ptx::tmem_ld32(lane_addr + kTmemO + cc * 32, ov);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence(ov);
-                uint32_t pk[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    pk[t] = empty ? 0u
-                                  : ptx::pack_bf16x2(__uint_as_float(ov[2 * t]) * inv,
-                                                     __uint_as_float(ov[2 * t + 1]) * inv);
-                if (orow) {
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        orow[cc * 4 + t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-                }
-            }
-            if (a.lse && i < a.Nq)
-                a.lse[((long long)b * a.H + h) * a.Nq + i] = empty ? -INFINITY : (m_run + log2f(l_run)) * kLn2;
+            write_row<DV>(lane_addr + kTmemO, l_run, m_run,
+                          (i < a.Nq) ? a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2 : nullptr,
+                          (a.lse && i < a.Nq) ? a.lse + ((long long)b * a.H + h) * a.Nq + i : nullptr);
         }
     }
 
@@ -539,13 +382,9 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 template <bool kBias>
 attn_status_t dispatch(int dk, int dv, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                        const Args &a, unsigned grid, cudaStream_t s) {
-    if (dk == 64 && dv == 64) return launch_t<64, 64, kBias>(mq, mk, mv, a, grid, s);
-    if (dk == 128 && dv == 128) return launch_t<128, 128, kBias>(mq, mk, mv, a, grid, s);
     if (dk == 192 && dv == 128) return launch_t<192, 128, kBias>(mq, mk, mv, a, grid, s);
-    if (dk == 128 && dv == 64) return launch_t<128, 64, kBias>(mq, mk, mv, a, grid, s);
-    if (dk == 64 && dv == 128) return launch_t<64, 128, kBias>(mq, mk, mv, a, grid, s);
     if (dk == 192 && dv == 64) return launch_t<192, 64, kBias>(mq, mk, mv, a, grid, s);
-    return fail(ATTN_ERR_UNSUPPORTED, "no bf16 kernel for dk=%d dv=%d", dk, dv);
+    return fail(ATTN_ERR_UNSUPPORTED, "no one-tile bf16 kernel for dk=%d dv=%d", dk, dv);
 }
 
 }  // namespace
@@ -566,9 +405,11 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
         mk = mq;  // never read: with no keys every tile is empty
         mv = mq;
     }
+    // dk <= 128: two query tiles per CTA; dk = 192: one (two would not fit in shared memory)
+    const bool pair = p.dk <= 128;
     Args a;
     a.B = (int)p.B; a.H = (int)p.H; a.Nq = (int)p.Nq; a.Nk = (int)p.Nk; a.causal = p.causal;
-    a.n_qt = (int)((p.Nq + BQ - 1) / BQ);
+    a.n_items = (int)((p.Nq + (pair ? 2 * BQ : BQ) - 1) / (pair ? 2 * BQ : BQ));
     a.scale_log2 = p.scale * kLog2e;
     a.o = static_cast<__nv_bfloat16 *>(p.o);
     a.os0 = p.o_stride[0]; a.os1 = p.o_stride[1]; a.os2 = p.o_stride[2];
@@ -577,7 +418,8 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     a.kv_lens = p.kv_lens;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
-    const long long grid = (long long)a.n_qt * p.B * p.H;
+    if (pair) return launch_fwd_bf16_pair(mq, mk, mv, a, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
+    const long long grid = (long long)a.n_items * p.B * p.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
     if (p.bias) return dispatch<true>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);
     return dispatch<false>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);

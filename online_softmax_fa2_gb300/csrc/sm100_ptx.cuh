@@ -207,6 +207,17 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Per-warpgroup register budget (whole warpgroup, same value).  The budgets of all
+// warpgroups must add up to no more than the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ descriptors
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and stride byte
