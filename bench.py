@@ -50,9 +50,13 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_sha(name):
-    with open(os.path.join(ROOT, "online_softmax_fa2_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_sha(*names):
+    """First 16 hex digits of the sha256 of the concatenated kernel sources."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "online_softmax_fa2_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(summary, source):
@@ -64,7 +68,7 @@ def profiled_traffic(summary, source):
     if not m:
         return None
     d = json.loads(m.group(1))
-    if d.get("source_sha256") != kernel_sha(source):
+    if d.get("source_sha256") != kernel_sha(*source):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -333,7 +337,7 @@ def run_ours(args):
                             "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                             "peak_kind": f"{pk_kind} copy bandwidth",
                             "traffic": profiled_traffic("decode_split_kernel.decode_b64_h32_l8192_d128.md",
-                                                        "decode.cu")}}
+                                                        ("decode.cu",))}}
         del d, ws
 
     line = {
@@ -350,8 +354,9 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                      "peak_kind": f"{pk_kind} dense bf16 (burst)",
-                     "traffic": profiled_traffic("fwd_bf16_kernel.causal_b4_h16_n2048_d128.md",
-                                                 "fwd_bf16_sm103.cu")},
+                     "kernel": "fwd_bf16_pair_kernel<128, 128, false>",
+                     "traffic": profiled_traffic("fwd_bf16_pair_kernel.causal_b4_h16_n2048_d128.md",
+                                                 ("fwd_bf16_pair_sm103.cu", "fwd_bf16_common.cuh"))},
         "clocks": clocks,
     }
     if dec:
