@@ -71,34 +71,53 @@ __device__ __forceinline__ void load_s_row(uint32_t taddr, float (&x)[BK]) {
     for (int k = 0; k < BK; ++k) x[k] = __uint_as_float(raw[k]);
 }
 
-// Turns a row of S into what the maximum is taken on and returns the tile maximum in base-2
-// units (-inf when no key of the tile is visible).  With a bias, x becomes the base-2 logit
-// S*c + b*log2(e); without one, x stays raw S and the scale is applied to the maximum only
-// (c > 0) and later inside the exponent.  Keys >= lim become -inf (a select: whatever is
-// stored at a masked position, NaN included, is dropped here).
-template <bool kBias>
-__device__ __forceinline__ float tile_logits(float (&x)[BK], float c, const float *bias_row,
-                                             bool bias_vec, int kv0, int n, bool need_mask,
-                                             int lim) {
-    if (kBias) {
+// Bias of this row for keys [kv0, kv0 + BK) in base-2 units (b * log2 e), written into xb;
+// keys >= n (masked in any case) read as 0 and are never loaded.  The loads have no consumer
+// until load_s_row_bias, so a call placed right after a tile's P is stored keeps them in
+// flight while the thread waits for the next S.
+__device__ __forceinline__ void load_bias(const float *bias_row, bool bias_vec, int kv0, int n,
+                                          float (&xb)[BK]) {
+    if (!bias_row) {
+#pragma unroll
+        for (int k = 0; k < BK; ++k) xb[k] = 0.f;
+        return;
+    }
+    if (bias_vec && kv0 + BK <= n) {
 #pragma unroll
         for (int k4 = 0; k4 < BK / 4; ++k4) {
-            float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int key = kv0 + 4 * k4;
-            if (bias_row && bias_vec && key + 3 < n)
-                bb = __ldg(reinterpret_cast<const float4 *>(bias_row + key));
-            else if (bias_row) {
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int e = 0; e < 4; ++e)
-                    if (key + e < n) t[e] = bias_row[key + e];
-                bb = make_float4(t[0], t[1], t[2], t[3]);
-            }
-            x[4 * k4 + 0] = fmaf(x[4 * k4 + 0], c, bb.x * kLog2e);
-            x[4 * k4 + 1] = fmaf(x[4 * k4 + 1], c, bb.y * kLog2e);
-            x[4 * k4 + 2] = fmaf(x[4 * k4 + 2], c, bb.z * kLog2e);
-            x[4 * k4 + 3] = fmaf(x[4 * k4 + 3], c, bb.w * kLog2e);
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(bias_row + kv0) + k4);
+            xb[4 * k4 + 0] = v.x * kLog2e;
+            xb[4 * k4 + 1] = v.y * kLog2e;
+            xb[4 * k4 + 2] = v.z * kLog2e;
+            xb[4 * k4 + 3] = v.w * kLog2e;
         }
+    } else {
+#pragma unroll
+        for (int k = 0; k < BK; ++k) xb[k] = (kv0 + k < n) ? __ldg(bias_row + kv0 + k) * kLog2e : 0.f;
     }
+}
+
+// x = S * c + xb in place: the row of S from TMEM columns [taddr, taddr + BK), 32 columns at a
+// time (so that S and the bias never need 256 registers at once).
+__device__ __forceinline__ void load_s_row_bias(uint32_t taddr, float c, float (&xb)[BK]) {
+#pragma unroll
+    for (int cc = 0; cc < BK / 32; ++cc) {
+        uint32_t t[32];
+        ptx::tmem_ld32(taddr + cc * 32, t);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(t);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) xb[cc * 32 + k] = fmaf(__uint_as_float(t[k]), c, xb[cc * 32 + k]);
+    }
+}
+
+// Masks keys >= lim (a select: whatever is stored at a masked position, NaN included, is
+// dropped here) and returns the tile maximum in base-2 units (-inf when no key of the tile is
+// visible).  With a bias, x already holds base-2 logits; without one, x is raw S and the
+// scale is applied to the maximum only (c > 0) and later inside the exponent.
+template <bool kBias>
+__device__ __forceinline__ float tile_logits(float (&x)[BK], float c, int kv0, bool need_mask,
+                                             int lim) {
     if (need_mask) {
 #pragma unroll
         for (int k = 0; k < BK; ++k)

@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim are visible
+            float x[BK];  // with a bias: the next tile's bias, loaded ahead
+            if (kBias) load_bias(bias_row, bias_vec, 0, n, x);
             for (int j = 0; j < nX; ++j) {
                 const int kv0 = j * BK;
                 if (!wait_warp(&ctrl->s_full[X], j & 1)) {
@@ -271,10 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                float x[BK];
-                load_s_row(lane_addr + s_col, x);
+                if (kBias) load_s_row_bias(lane_addr + s_col, c, x);
+                else load_s_row(lane_addr + s_col, x);
                 const bool need_mask = (kv0 + BK > n) || (a.causal && kv0 + BK - 1 > r0 + shift);
-                const float mt = tile_logits<kBias>(x, c, bias_row, bias_vec, kv0, n, need_mask, lim);
+                const float mt = tile_logits<kBias>(x, c, kv0, need_mask, lim);
                 bool rescale;
                 const float alpha = update_max(mt, m_run, rescale);
                 const float lsum = tile_exp<kBias>(x, c, m_run);
@@ -294,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 store_p(lane_addr + s_col, x);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&ctrl->p_full[X]);
+                if (kBias && j + 1 < nX) load_bias(bias_row, bias_vec, kv0 + BK, n, x);
             }
             if (ok && wait_warp(&ctrl->o_final[X], 0)) {
                 ptx::tc_fence_after();

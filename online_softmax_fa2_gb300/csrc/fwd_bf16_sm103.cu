@@ -266,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __all_sync(0xffffffffu, w);
         };
 
+        float x[BK];  // with a bias: the next tile's bias, loaded ahead
+        if (kBias) load_bias(bias_row, bias_vec, 0, n, x);
         for (int j = 0; j < n_tiles; ++j) {
             const int buf = j % kSBufs, kv0 = j * BK;
             if (!wait_warp(&ctrl->s_full[buf], (j / kSBufs) & 1)) {
@@ -273,11 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            float x[BK];
-            load_s_row(lane_addr + buf * BK, x);
+            if (kBias) load_s_row_bias(lane_addr + buf * BK, c, x);
+            else load_s_row(lane_addr + buf * BK, x);
             const bool need_mask = (kv0 + BK > n) || (a.causal && kv0 + BK - 1 > q0 + shift);
             const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim visible
-            const float mt = tile_logits<kBias>(x, c, bias_row, bias_vec, kv0, n, need_mask, lim);
+            const float mt = tile_logits<kBias>(x, c, kv0, need_mask, lim);
             bool rescale;
             const float alpha = update_max(mt, m_run, rescale);
             const float lsum = tile_exp<kBias>(x, c, m_run);
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_p(lane_addr + buf * BK, x);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&ctrl->p_full[buf]);
+            if (kBias && j + 1 < n_tiles) load_bias(bias_row, bias_vec, kv0 + BK, n, x);
         }
 
         // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf
