@@ -12,13 +12,13 @@
 //   warp 0       TMA producer: Q_A and Q_B once, then K and V tiles into two rings.
 //   warp 1       tensor-core issuer (one thread); owns the 512 TMEM columns:
 //                  S_A/P_A [0,128)  S_B/P_B [128,256)  O_A [256,384)  O_B [384,512).
-//                Per key tile j: O_A += P_A V_j, then (once that product has completed and
-//                so no longer reads P_A) S_A(j+1) = Q_A K_{j+1}^T into the same columns;
-//                then the same for B.
+//                Per key tile j: O_A += P_A V_j, then S_A(j+1) = Q_A K_{j+1}^T into the
+//                same columns (tcgen05.mma operations from one thread execute in issue
+//                order, so the product reads P_A before the next S overwrites it); then B.
 //   warps 4-7    softmax of tile A, one thread per query row (its TMEM lane).
 //   warps 8-11   softmax of tile B.
-// Because S_X(j+1) is issued only after P_X(j) V_j has completed, a softmax thread that sees
-// S_X(j+1) may rescale O_X directly: no product is writing it.
+// The commit behind S_X(j+1) covers P_X(j) V_j, so a softmax thread that sees S_X(j+1) may
+// rescale O_X directly: no product is writing it.
 //
 // The per-row steps (mask, maximum, exponentials, rescale, one division at the end) are those
 // of fwd_bf16_common.cuh; masking and the empty-row policy are as in the one-tile kernel.
@@ -40,7 +40,7 @@ constexpr int kMaxStages = 4;
 struct Ctrl {
     uint64_t q_full;
     uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
-    uint64_t s_full[2], p_full[2], pv_done[2], o_final[2];
+    uint64_t s_full[2], p_full[2], o_final[2];
     uint64_t final_mma;
     uint32_t tmem_base;
     int abort;
@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(&ctrl->s_full[t], 1);
             ptx::mbar_init(&ctrl->p_full[t], BQ);
-            ptx::mbar_init(&ctrl->pv_done[t], 1);
             ptx::mbar_init(&ctrl->o_final[t], 1);
         }
         ptx::mbar_init(&ctrl->final_mma, 1);
@@ -223,15 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_ts(tmem + 2 * BQ + t * BQ, tmem + t * BQ + kk * 8,
                                     ptx::sdesc_sw128(v_addr + kk * 16 * 128, kPanelBytes, 1024), kIdO,
                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(&ctrl->pv_done[t]);
                     if (j == nt - 1) ptx::mma_commit(&ctrl->o_final[t]);
-                    if (j + 1 < nt) {
-                        // P_t(j) is read by the product just issued: reuse its columns for
-                        // S_t(j+1) only once that product has completed
-                        if (!wait(&ctrl->pv_done[t], j & 1) || !issue_s(t, j + 1)) {
-                            ok = false;
-                            break;
-                        }
+                    // S_t(j+1) overwrites the columns P_t(j) occupies: tcgen05.mma operations
+                    // issued by one thread execute in issue order, so the product just issued
+                    // has read P_t(j) before S_t(j+1) is written; and the commit behind
+                    // s_full[t] covers that product, so O_t is complete when the softmax sees
+                    // S_t(j+1).
+                    if (j + 1 < nt && !issue_s(t, j + 1)) {
+                        ok = false;
+                        break;
                     }
                 }
                 if (!ok) break;
