@@ -226,6 +226,39 @@ __device__ __forceinline__ void write_row(uint32_t taddr, float l_run, float m_r
     if (lse_out) *lse_out = empty ? -INFINITY : (m_run + log2f(l_run)) * kLn2;
 }
 
+// As write_row, but the bf16 row goes into a shared-memory staging tile laid out like a TMA
+// box of 128 rows x 64 columns per panel with the 128-byte swizzle (16-byte chunk c of row r
+// at chunk c ^ (r & 7)), for a bulk-tensor store; row r's eight chunks fall in eight
+// different bank groups, so a warp's writes do not conflict.
+template <int DV>
+__device__ __forceinline__ void stage_row(uint32_t taddr, float l_run, float m_run, uint8_t *stage,
+                                          int r, float *lse_out) {
+    const bool empty = !(l_run > 0.f);
+    const float inv = empty ? 0.f : 1.f / l_run;
+#pragma unroll
+    for (int cc = 0; cc < DV / 32; ++cc) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(taddr + cc * 32, ov);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            pk[t] = empty ? 0u
+                          : ptx::pack_bf16x2(__uint_as_float(ov[2 * t]) * inv,
+                                             __uint_as_float(ov[2 * t + 1]) * inv);
+        // columns [32 cc, 32 cc + 32) = panel cc / 2, chunks 4 (cc % 2) .. 4 (cc % 2) + 3
+        uint8_t *row = stage + (cc / 2) * kPanelBytes + r * 128;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int chunk = (cc % 2) * 4 + t;
+            *reinterpret_cast<uint4 *>(row + ((chunk ^ (r & 7)) * 16)) =
+                make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+    }
+    if (lse_out) *lse_out = empty ? -INFINITY : (m_run + log2f(l_run)) * kLn2;
+}
+
 // A row that sees no key at all: o = +0.0, lse = -inf (no TMEM involved).
 template <int DV>
 __device__ __forceinline__ void write_empty_row(__nv_bfloat16 *orow, float *lse_out) {
@@ -252,7 +285,8 @@ __device__ __forceinline__ void zero_v_row(uint8_t *sV, int row) {
 
 // Launches the two-tile kernel (dk <= 128); defined in fwd_bf16_pair_sm103.cu.
 attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
-                                   const CUtensorMap &mv, const bf16fwd::Args &a, int dk, int dv,
-                                   bool bias, cudaStream_t s);
+                                   const CUtensorMap &mv, const CUtensorMap &mo,
+                                   const bf16fwd::Args &a, int dk, int dv, bool bias,
+                                   cudaStream_t s);
 
 }  // namespace attn

@@ -40,7 +40,7 @@ constexpr int kMaxStages = 4;
 struct Ctrl {
     uint64_t q_full;
     uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
-    uint64_t s_full[2], p_full[2], o_final[2];
+    uint64_t s_full[2], p_full[2], o_final[2], o_staged[2];
     uint64_t final_mma;
     uint32_t tmem_base;
     int abort;
@@ -70,7 +70,8 @@ template <int DK, int DV, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const Args a) {
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_o, const Args a) {
     using L = Layout<DK, DV>;
     constexpr int KS = L::kKStages, VS = L::kVStages;
     extern __shared__ uint8_t smem_raw[];
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&ctrl->s_full[t], 1);
             ptx::mbar_init(&ctrl->p_full[t], BQ);
             ptx::mbar_init(&ctrl->o_final[t], 1);
+            ptx::mbar_init(&ctrl->o_staged[t], BQ);
         }
         ptx::mbar_init(&ctrl->final_mma, 1);
         ctrl->abort = 0;
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_o);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&ctrl->tmem_base, kTmemCols);
@@ -299,7 +302,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok && wait_warp(&ctrl->o_final[X], 0)) {
                 ptx::tc_fence_after();
-                write_row<DV>(lane_addr + o_col, l_run, m_run, orow, lse_out);
+                if constexpr (DV <= DK) {
+                    // divide once, stage the bf16 tile in Q_X's shared memory (its last reader,
+                    // S_X of the last key tile, completed before o_final) and store it with TMA
+                    uint8_t *stage = smem + X * L::kQBytes;
+                    stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, lse_out);
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(&ctrl->o_staged[X]);
+                    // one thread stores the tile once all 128 rows are staged (a bounded wait:
+                    // a warp that gave up earlier never arrives, and the store is then skipped)
+                    if (r == 0 && ptx::mbar_wait(&ctrl->o_staged[X], 0, abort, a.flags,
+                                                 kFlagWaitTimeout, kWaitLimitNs)) {
+#pragma unroll
+                        for (int p = 0; p < DV / 64; ++p)
+                            ptx::tma_store_4d(&tm_o, stage + p * kPanelBytes, p * 64, r0, h, b);
+                        ptx::bulk_commit();
+                        ptx::bulk_wait_read();
+                    }
+                } else {
+                    write_row<DV>(lane_addr + o_col, l_run, m_run, orow, lse_out);
+                }
             }
         }
     }
@@ -315,14 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DK, int DV, bool kBias>
 attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                       const Args &a, cudaStream_t s) {
+                       const CUtensorMap &mo, const Args &a, cudaStream_t s) {
     const int smem = Layout<DK, DV>::kBytes;
     auto kern = fwd_bf16_pair_kernel<DK, DV, kBias>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const long long grid = (long long)a.n_items * a.B * a.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, mo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16_pair launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
@@ -331,11 +353,13 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 }  // namespace
 
 attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
-                                   const CUtensorMap &mv, const bf16fwd::Args &a, int dk, int dv,
-                                   bool bias, cudaStream_t s) {
+                                   const CUtensorMap &mv, const CUtensorMap &mo,
+                                   const bf16fwd::Args &a, int dk, int dv, bool bias,
+                                   cudaStream_t s) {
 #define ATTN_PAIR_CASE(DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_)                                                                \
-        return bias ? launch_t<DK_, DV_, true>(mq, mk, mv, a, s) : launch_t<DK_, DV_, false>(mq, mk, mv, a, s);
+        return bias ? launch_t<DK_, DV_, true>(mq, mk, mv, mo, a, s)                           \
+                    : launch_t<DK_, DV_, false>(mq, mk, mv, mo, a, s);
     ATTN_PAIR_CASE(128, 128)
     ATTN_PAIR_CASE(64, 64)
     ATTN_PAIR_CASE(128, 64)

@@ -421,7 +421,11 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     a.kv_lens = p.kv_lens;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
-    if (pair) return launch_fwd_bf16_pair(mq, mk, mv, a, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
+    if (pair) {
+        CUtensorMap mo;
+        if ((st = encode(&mo, p.o, p.B, p.Nq, p.H, p.dv, p.o_stride, "o"))) return st;
+        return launch_fwd_bf16_pair(mq, mk, mv, mo, a, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
+    }
     const long long grid = (long long)a.n_items * p.B * p.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
     if (p.bias) return dispatch<true>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);
