@@ -153,17 +153,22 @@ __device__ __forceinline__ float update_max(float mt, float &m_run, bool &rescal
     return 1.f;
 }
 
-// p = 2^(x - m) in place (one FFMA + one ex2 per element); returns the row's tile mass.
+// p = 2^(x - m) in place (half a packed FFMA + one ex2 per element); returns the row's
+// tile mass.
 template <bool kBias>
 __device__ __forceinline__ float tile_exp(float (&x)[BK], float c, float m_run) {
     const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+    const float cc = kBias ? 1.f : c;
     float s8[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) s8[t] = 0.f;
+    // two elements per packed f32x2 FMA and add: half the FP32 instructions of the softmax
 #pragma unroll
-    for (int k = 0; k < BK; ++k) {
-        x[k] = kBias ? ptx::ex2(x[k] - mref) : ptx::ex2(fmaf(x[k], c, -mref));
-        s8[k & 7] += x[k];
+    for (int k = 0; k < BK; k += 2) {
+        ptx::fma2(x[k], x[k + 1], x[k], x[k + 1], cc, cc, -mref, -mref);
+        x[k] = ptx::ex2(x[k]);
+        x[k + 1] = ptx::ex2(x[k + 1]);
+        ptx::add2(s8[k & 7], s8[(k & 7) + 1], s8[k & 7], s8[(k & 7) + 1], x[k], x[k + 1]);
     }
     return ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
 }
