@@ -63,32 +63,42 @@ struct Ctrl {
     uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
     uint64_t o_done;     // one completion per P V product (O rescale waits on PV_{j-1})
     uint64_t o_final;    // completes once, after the last P V product
+    uint64_t b_full, b_empty;  // bias tile staged by TMA (bias kernels with a TMA-able bias)
     uint64_t final_mma;
     uint32_t tmem_base;
     int abort;
 };
 
-template <int DK, int DV>
+// kTmaBias: the bias tile (128 rows x 128 keys fp32, four 32-key panels, 128-byte swizzled)
+// is staged in shared memory by TMA; one K and one V stage then make room for it.
+constexpr int kBiasBytes = 4 * kPanelBytes;
+
+template <int DK, int DV, bool kTmaBias = false>
 struct Layout {
     static constexpr int kQBytes = (DK / 64) * kPanelBytes;
     static constexpr int kKBytes = (DK / 64) * kPanelBytes;
     static constexpr int kVBytes = (DV / 64) * kPanelBytes;
-    // deepest equal K and V rings that fit next to Q
+    static constexpr int kFixed = kQBytes + (kTmaBias ? kBiasBytes : 0) + 2048;
+    // deepest equal K and V rings that fit next to Q (and the bias tile)
     static constexpr int kStages =
-        (kQBytes + 4 * (kKBytes + kVBytes) + 2048 <= kSmemMax) ? 4
-        : (kQBytes + 3 * (kKBytes + kVBytes) + 2048 <= kSmemMax) ? 3 : 2;
+        (kFixed + 4 * (kKBytes + kVBytes) <= kSmemMax) ? 4
+        : (kFixed + 3 * (kKBytes + kVBytes) <= kSmemMax) ? 3
+        : (kFixed + 2 * (kKBytes + kVBytes) <= kSmemMax) ? 2 : 1;
     static constexpr int kKOff = kQBytes;                       // K ring
     static constexpr int kVOff = kQBytes + kStages * kKBytes;   // V ring
-    static constexpr int kDataBytes = kVOff + kStages * kVBytes;
+    static constexpr int kBOff = kVOff + kStages * kVBytes;     // bias tile
+    static constexpr int kDataBytes = kBOff + (kTmaBias ? kBiasBytes : 0);
     static constexpr int kBytes = kDataBytes + (int)sizeof(Ctrl) + 1024;  // + alignment slack
     static_assert(kBytes <= kSmemMax, "shared memory budget");
 };
 
-template <int DK, int DV, bool kBias>
+template <int DK, int DV, bool kBias, bool kTmaBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Args a) {
-    using L = Layout<DK, DV>;
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_b,
+                    const Args a) {
+    static_assert(kBias || !kTmaBias, "a staged bias needs a bias");
+    using L = Layout<DK, DV, kTmaBias>;
     constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -132,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(&ctrl->o_done, 1);
         ptx::mbar_init(&ctrl->o_final, 1);
+        ptx::mbar_init(&ctrl->b_full, 1);
+        ptx::mbar_init(&ctrl->b_empty, 128);
         ptx::mbar_init(&ctrl->final_mma, 1);
         ctrl->abort = 0;
         ptx::fence_mbar_init();
@@ -140,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
+        if (kTmaBias) ptx::prefetch_tmap(&tm_b);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&ctrl->tmem_base, kTmemCols);
@@ -157,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int p = 0; p < DK / 64; ++p)
                 ptx::tma_load_4d(sQ + p * kPanelBytes, &tm_q, &ctrl->q_full, p * 64, q0, h, b);
-            int last_k = -1, last_v = -1;  // last tiles whose K / V copies were issued
+            int last_k = -1, last_v = -1, last_b = -1;  // last tiles whose copies were issued
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kStages;
                 if (j >= kStages &&
@@ -171,6 +184,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int p = 0; p < DK / 64; ++p)
                     ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[st], p * 64, j * BK, h, b);
                 last_k = j;
+                if (kTmaBias) {
+                    // bias tile j, as soon as the softmax has read tile j-1 (ahead of V_j, which
+                    // waits for the previous P V product)
+                    if (j >= 1 && !ptx::mbar_wait(&ctrl->b_empty, (j - 1) & 1, abort, a.flags,
+                                                  kFlagWaitTimeout, kWaitLimitNs))
+                        break;
+                    ptx::mbar_arrive_expect_tx(&ctrl->b_full, kBiasBytes);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        ptx::tma_load_4d(smem + L::kBOff + p * kPanelBytes, &tm_b, &ctrl->b_full,
+                                         j * BK + 32 * p, q0, h, b);
+                    last_b = j;
+                }
                 if (j >= kStages &&
                     !ptx::mbar_wait(&ctrl->v_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
@@ -187,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_wait_quiet(&ctrl->k_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
                 for (int j = max(0, last_v - kStages + 1); j <= last_v; ++j)
                     ptx::mbar_wait_quiet(&ctrl->v_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
+                if (last_b >= 0) ptx::mbar_wait_quiet(&ctrl->b_full, last_b & 1, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
@@ -267,9 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         float x[BK];  // with a bias: the next tile's bias, loaded ahead
-        if (kBias) load_bias(bias_row, bias_vec, 0, n, x);
+        if (kBias && !kTmaBias) load_bias(bias_row, bias_vec, 0, n, x);
         for (int j = 0; j < n_tiles; ++j) {
             const int buf = j % kSBufs, kv0 = j * BK;
+            if (kTmaBias) {  // this tile's bias row from the staged tile, then free the stage
+                if (!wait_warp(&ctrl->b_full, j & 1)) {
+                    ok = false;
+                    break;
+                }
+                read_bias_stage(smem + L::kBOff, r, x);
+                ptx::mbar_arrive(&ctrl->b_empty);
+            }
             if (!wait_warp(&ctrl->s_full[buf], (j / kSBufs) & 1)) {
                 ok = false;
                 break;
@@ -312,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_p(lane_addr + buf * BK, x);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&ctrl->p_full[buf]);
-            if (kBias && j + 1 < n_tiles) load_bias(bias_row, bias_vec, kv0 + BK, n, x);
+            if (kBias && !kTmaBias && j + 1 < n_tiles) load_bias(bias_row, bias_vec, kv0 + BK, n, x);
         }
 
         // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf
@@ -368,25 +403,47 @@ attn_status_t encode(CUtensorMap *m, const void *ptr, int64_t B, int64_t N, int6
     return ATTN_OK;
 }
 
-template <int DK, int DV, bool kBias>
-attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const Args &a,
-                       unsigned grid, cudaStream_t s) {
-    int smem = Layout<DK, DV>::kBytes;
+// 4-D map over the fp32 bias [B, H, Nq, Nk] (key stride 1, element strides bs: b, h, i);
+// box 32 keys x 128 rows, 128-byte swizzle.  Returns false when the bias does not meet the
+// TMA rules (16-byte aligned base, strides that are non-zero multiples of 16 bytes).
+bool encode_bias(CUtensorMap *m, const attn_fwd_params_t &p) {
+    auto enc = get_encoder();
+    if (!enc || (reinterpret_cast<uintptr_t>(p.bias) & 15u)) return false;
+    const int64_t sizes[3] = {p.B, p.H, p.Nq};
+    for (int t = 0; t < 3; ++t)
+        if (sizes[t] > 1 && (p.bias_stride[t] <= 0 || p.bias_stride[t] % 4)) return false;
+    auto bstride = [](int64_t st, int64_t size) -> cuuint64_t {
+        return size <= 1 ? 16u : (cuuint64_t)(st * 4);
+    };
+    cuuint64_t dims[4] = {(cuuint64_t)p.Nk, (cuuint64_t)p.Nq, (cuuint64_t)p.H, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {bstride(p.bias_stride[2], p.Nq), bstride(p.bias_stride[1], p.H),
+                             bstride(p.bias_stride[0], p.B)};
+    cuuint32_t box[4] = {32, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(p.bias), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DK, int DV, bool kBias, bool kTmaBias>
+attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                       const CUtensorMap &mb, const Args &a, unsigned grid, cudaStream_t s) {
+    int smem = Layout<DK, DV, kTmaBias>::kBytes;
     if (smem < 116 * 1024) smem = 116 * 1024;  // one CTA per SM: it owns all 512 TMEM columns
-    auto kern = fwd_bf16_kernel<DK, DV, kBias>;
+    auto kern = fwd_bf16_kernel<DK, DV, kBias, kTmaBias>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mb, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16 launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }
 
-template <bool kBias>
+template <bool kBias, bool kTmaBias>
 attn_status_t dispatch(int dk, int dv, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                       const Args &a, unsigned grid, cudaStream_t s) {
-    if (dk == 192 && dv == 128) return launch_t<192, 128, kBias>(mq, mk, mv, a, grid, s);
-    if (dk == 192 && dv == 64) return launch_t<192, 64, kBias>(mq, mk, mv, a, grid, s);
+                       const CUtensorMap &mb, const Args &a, unsigned grid, cudaStream_t s) {
+    if (dk == 192 && dv == 128) return launch_t<192, 128, kBias, kTmaBias>(mq, mk, mv, mb, a, grid, s);
+    if (dk == 192 && dv == 64) return launch_t<192, 64, kBias, kTmaBias>(mq, mk, mv, mb, a, grid, s);
     return fail(ATTN_ERR_UNSUPPORTED, "no one-tile bf16 kernel for dk=%d dv=%d", dk, dv);
 }
 
@@ -428,8 +485,11 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     }
     const long long grid = (long long)a.n_items * p.B * p.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
-    if (p.bias) return dispatch<true>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);
-    return dispatch<false>((int)p.dk, (int)p.dv, mq, mk, mv, a, (unsigned)grid, s);
+    CUtensorMap mb = mq;  // read only by kernels that stage the bias
+    if (p.bias && p.Nk > 0 && encode_bias(&mb, p))
+        return dispatch<true, true>((int)p.dk, (int)p.dv, mq, mk, mv, mb, a, (unsigned)grid, s);
+    if (p.bias) return dispatch<true, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, a, (unsigned)grid, s);
+    return dispatch<false, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, a, (unsigned)grid, s);
 }
 
 }  // namespace attn

@@ -122,6 +122,30 @@ def test_bf16_padding_bias_and_bias_masks(causal):
     compare(o, lse, o_ref, l_ref, torch.bfloat16, what="bias+padding")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nk", [392, 1024])
+def test_bf16_dk192_bias_staged_by_tma(causal, Nk):
+    # bias rows 16-byte aligned (Nk a multiple of 4): the bias tile goes through TMA
+    a = wl.make_prefill(3, 2, 300, Nk, 192, 128, torch.bfloat16, causal=causal, bias=True,
+                        kv_lens=[Nk, 129, Nk - 1], seed=28, device=DEV, bias_mask_p=0.05)
+    o, lse = run(a)
+    o_ref, l_ref, _ = oracle_full(a)
+    compare(o, lse, o_ref, l_ref, torch.bfloat16, what=f"staged bias Nk={Nk}")
+
+
+def test_bf16_dk192_staged_bias_masked_positions_bit_exact():
+    kw = dict(B=3, H=2, Nq=257, Nk=336, dk=192, dv=128, dtype=torch.bfloat16, causal=True,
+              bias=True, kv_lens=[336, 150, 77], seed=29, device=DEV)
+    clean = wl.make_prefill(**kw, poison=False)
+    dirty = wl.make_prefill(**kw, poison=True)
+    o1, l1 = run(clean)
+    o2, l2 = run(dirty)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+    o_ref, l_ref, _ = oracle_full(clean)
+    compare(o2, l2, o_ref, l_ref, torch.bfloat16, what="staged bias, poisoned")
+
+
 def test_bf16_masked_positions_bit_exact():
     # NaN stored at every masked position (keys/values past kv_len, bias at masked (i, j))
     # must leave every output bit unchanged
