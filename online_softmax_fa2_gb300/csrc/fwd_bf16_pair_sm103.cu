@@ -1,15 +1,20 @@
 // fwd_bf16_pair_sm103.cu -- bf16 attention forward, two 128-row query tiles per CTA.
 //
-// A CTA owns 256 consecutive query rows of one (b, h): tile A (rows q0..q0+127) and tile B
-// (rows q0+128..q0+255).  Every K and V tile brought into shared memory serves both query
-// tiles, which halves the key/value traffic per FLOP against one tile per CTA, and the two
+// A work item is 256 consecutive query rows of one (b, h): tile A (rows q0..q0+127) and tile
+// B (rows q0+128..q0+255).  Every K and V tile brought into shared memory serves both query
+// tiles, which halves the key/value traffic per FLOP against one tile per item, and the two
 // tiles' softmax warpgroups take turns with the tensor cores: while one warpgroup turns its
 // S into P, the tensor cores compute the other tile's products ("How Does FlashAttention
 // Preserve Global Softmax Across Tiles?", section 5: every query row keeps its own state;
-// section 8: query-block parallelism).  Work items are numbered longest first.
+// section 8: query-block parallelism).
+//
+// The kernel is persistent: one CTA per SM walks a fixed list of items, numbered longest
+// first and dealt out in rows taken in alternating direction.  Barrier phases run on from one
+// item to the next, so the next item's Q and first K/V tiles load, and its first S products
+// run, while the softmax warpgroups are still writing the previous item's rows.
 //
 // Roles (384 threads = 3 warpgroups):
-//   warp 0       TMA producer: Q_A and Q_B once, then K and V tiles into two rings.
+//   warp 0       TMA producer: per item Q_A and Q_B, then K and V tiles into two rings.
 //   warp 1       tensor-core issuer (one thread); owns the 512 TMEM columns:
 //                  S_A/P_A [0,128)  S_B/P_B [128,256)  O_A [256,384)  O_B [384,512).
 //                Per key tile j: O_A += P_A V_j, then S_A(j+1) = Q_A K_{j+1}^T into the
@@ -38,7 +43,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStages = 4;
 
 struct Ctrl {
-    uint64_t q_full;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], o_final[2], o_staged[2];
     uint64_t final_mma;
@@ -66,6 +71,33 @@ struct Layout {
     static_assert(kBytes <= kSmemMax, "shared memory budget");
 };
 
+// Work item k (0 <= k < B * H * n_items, numbered longest first) -> (b, h, 256-row block).
+struct Item {
+    int b, h, q0, n, nA, nB, nmax;
+};
+
+__device__ __forceinline__ Item decode_item(const Args &a, int k, bool report) {
+    Item it;
+    const int bhn = a.B * a.H;
+    const int blk = a.n_items - 1 - k / bhn;  // later query blocks see more keys: first
+    const int bh = k % bhn;
+    it.b = bh / a.H;
+    it.h = bh % a.H;
+    it.q0 = blk * 2 * BQ;
+    it.n = seq_len(a, it.b, report && blk == 0 && it.h == 0);
+    it.nA = kv_tiles(a, it.q0, it.n);
+    it.nB = kv_tiles(a, it.q0 + BQ, it.n);
+    it.nmax = max(it.nA, it.nB);
+    return it;
+}
+
+// The r-th item of CTA c among G resident CTAs: rows of G consecutive items of the
+// longest-first list, taken in alternating direction (c, then G-1-c, ...), so that each CTA's
+// total is close to the mean.
+__device__ __forceinline__ int item_index(int r, int c, int G) {
+    return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
 template <int DK, int DV, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -74,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_o, const Args a) {
     using L = Layout<DK, DV>;
     constexpr int KS = L::kKStages, VS = L::kVStages;
+    constexpr bool kStageA = DV <= DK;  // tile A's output fits in its Q buffer
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -81,30 +114,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort = &ctrl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bhn = a.B * a.H;
-    const int item = a.n_items - 1 - (int)(blockIdx.x / bhn);  // longest first
-    const int bh = (int)(blockIdx.x % bhn), b = bh / a.H, h = bh % a.H;
-    const int q0 = item * 2 * BQ;
-    const int n = seq_len(a, b, threadIdx.x == 0 && item == 0 && h == 0);
-    const int shift = n - a.Nq;
-    const int nA = kv_tiles(a, q0, n), nB = kv_tiles(a, q0 + BQ, n);
-    const int nmax = max(nA, nB);
-
-    // softmax thread's row (warps 4..11) and tile
-    const int X = (warp >= 8) ? 1 : 0;
-    const int r = (int)threadIdx.x - 128 - X * BQ;
-    const int i = q0 + X * BQ + r;
-    const int nX = X ? nB : nA;
-
-    if (nmax == 0) {  // every row of both tiles is empty
-        if (warp >= 4 && i < a.Nq)
-            write_empty_row<DV>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2,
-                                a.lse ? a.lse + ((long long)b * a.H + h) * a.Nq + i : nullptr);
-        return;
-    }
+    const int total = a.B * a.H * a.n_items;
+    const int G = (int)gridDim.x, cta = (int)blockIdx.x;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&ctrl->q_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(&ctrl->q_full[t], 1);
+            // Q_A is released by its last S product and by tile A's output store, which is
+            // staged in the same buffer when it fits (dv <= dk); Q_B by its last S product
+            ptx::mbar_init(&ctrl->q_empty[t], (t == 0 && kStageA) ? 2 : 1);
+            ptx::mbar_init(&ctrl->o_staged[t], BQ);
+            ptx::mbar_init(&ctrl->s_full[t], 1);
+            ptx::mbar_init(&ctrl->p_full[t], BQ);
+            ptx::mbar_init(&ctrl->o_final[t], 1);
+        }
         for (int s = 0; s < KS; ++s) {
             ptx::mbar_init(&ctrl->k_full[s], 1);
             ptx::mbar_init(&ctrl->k_empty[s], 1);
@@ -112,12 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < VS; ++s) {
             ptx::mbar_init(&ctrl->v_full[s], 1);
             ptx::mbar_init(&ctrl->v_empty[s], 1);
-        }
-        for (int t = 0; t < 2; ++t) {
-            ptx::mbar_init(&ctrl->s_full[t], 1);
-            ptx::mbar_init(&ctrl->p_full[t], BQ);
-            ptx::mbar_init(&ctrl->o_final[t], 1);
-            ptx::mbar_init(&ctrl->o_staged[t], BQ);
         }
         ptx::mbar_init(&ctrl->final_mma, 1);
         ctrl->abort = 0;
@@ -138,49 +155,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
 
+    // Barrier phases run on from one item to the next: g counts key tiles (K/V ring slots),
+    // and per query tile, Q loads, S/P hand-offs and finished items are counted likewise.
     if (warp < 4) {
       ptx::regs_dec<kRegsIssue>();
       if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(&ctrl->q_full, 2 * L::kQBytes);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int p = 0; p < DK / 64; ++p)
-                    ptx::tma_load_4d(smem + t * L::kQBytes + p * kPanelBytes, &tm_q, &ctrl->q_full,
-                                     p * 64, q0 + t * BQ, h, b);
-            int last_k = -1, last_v = -1;
-            for (int j = 0; j < nmax; ++j) {
-                const int ks = j % KS, vs = j % VS;
-                if (j >= KS && !ptx::mbar_wait(&ctrl->k_empty[ks], ((j / KS) - 1) & 1, abort,
-                                               a.flags, kFlagWaitTimeout, kWaitLimitNs))
-                    break;
-                uint8_t *sK = smem + L::kKOff + ks * L::kKBytes;
-                ptx::mbar_arrive_expect_tx(&ctrl->k_full[ks], L::kKBytes);
+            int g = 0, nqA = 0, nqB = 0, last_k = -1, last_v = -1;
+            // Q_t of the next item, once the previous item's last S_t has read the buffer
+            auto load_q = [&](int t, int &nq, const Item &it) -> bool {
+                if (nq > 0 && !ptx::mbar_wait(&ctrl->q_empty[t], (nq - 1) & 1, abort, a.flags,
+                                              kFlagWaitTimeout, kWaitLimitNs))
+                    return false;
+                ptx::mbar_arrive_expect_tx(&ctrl->q_full[t], L::kQBytes);
 #pragma unroll
                 for (int p = 0; p < DK / 64; ++p)
-                    ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[ks], p * 64, j * BK, h, b);
-                last_k = j;
-                if (j >= VS && !ptx::mbar_wait(&ctrl->v_empty[vs], ((j / VS) - 1) & 1, abort,
-                                               a.flags, kFlagWaitTimeout, kWaitLimitNs))
-                    break;
-                uint8_t *sV = smem + L::kVOff + vs * L::kVBytes;
-                ptx::mbar_arrive_expect_tx(&ctrl->v_full[vs], L::kVBytes);
+                    ptx::tma_load_4d(smem + t * L::kQBytes + p * kPanelBytes, &tm_q, &ctrl->q_full[t],
+                                     p * 64, it.q0 + t * BQ, it.h, it.b);
+                ++nq;
+                return true;
+            };
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int k = item_index(r, cta, G);
+                if (k >= total) break;
+                const Item it = decode_item(a, k, false);
+                if (it.nmax == 0) continue;
+                if (it.nA > 0 && !load_q(0, nqA, it)) break;
+                if (it.nB > 0 && !load_q(1, nqB, it)) break;
+                for (int j = 0; ok && j < it.nmax; ++j) {
+                    const int gj = g + j, ks = gj % KS, vs = gj % VS;
+                    if (gj >= KS && !ptx::mbar_wait(&ctrl->k_empty[ks], ((gj / KS) - 1) & 1, abort,
+                                                    a.flags, kFlagWaitTimeout, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sK = smem + L::kKOff + ks * L::kKBytes;
+                    ptx::mbar_arrive_expect_tx(&ctrl->k_full[ks], L::kKBytes);
 #pragma unroll
-                for (int p = 0; p < DV / 64; ++p)
-                    ptx::tma_load_4d(sV + p * kPanelBytes, &tm_v, &ctrl->v_full[vs], p * 64, j * BK, h, b);
-                last_v = j;
+                    for (int p = 0; p < DK / 64; ++p)
+                        ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[ks], p * 64, j * BK,
+                                         it.h, it.b);
+                    last_k = gj;
+                    if (gj >= VS && !ptx::mbar_wait(&ctrl->v_empty[vs], ((gj / VS) - 1) & 1, abort,
+                                                    a.flags, kFlagWaitTimeout, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sV = smem + L::kVOff + vs * L::kVBytes;
+                    ptx::mbar_arrive_expect_tx(&ctrl->v_full[vs], L::kVBytes);
+#pragma unroll
+                    for (int p = 0; p < DV / 64; ++p)
+                        ptx::tma_load_4d(sV + p * kPanelBytes, &tm_v, &ctrl->v_full[vs], p * 64, j * BK,
+                                         it.h, it.b);
+                    last_v = gj;
+                }
+                g += it.nmax;
             }
             if (*abort) {  // let copies still in flight land before the CTA exits
-                ptx::mbar_wait_quiet(&ctrl->q_full, 0, kWaitLimitNs);
+                if (nqA > 0) ptx::mbar_wait_quiet(&ctrl->q_full[0], (nqA - 1) & 1, kWaitLimitNs);
+                if (nqB > 0) ptx::mbar_wait_quiet(&ctrl->q_full[1], (nqB - 1) & 1, kWaitLimitNs);
                 for (int j = max(0, last_k - KS + 1); j <= last_k; ++j)
                     ptx::mbar_wait_quiet(&ctrl->k_full[j % KS], (j / KS) & 1, kWaitLimitNs);
                 for (int j = max(0, last_v - VS + 1); j <= last_v; ++j)
                     ptx::mbar_wait_quiet(&ctrl->v_full[j % VS], (j / VS) & 1, kWaitLimitNs);
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------ tensor-core issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BQ, BK, false);
@@ -189,56 +231,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto wait = [&](uint64_t *bar, uint32_t parity) {
                 return ptx::mbar_wait(bar, parity, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
             };
-            // S_t(j) = Q_t K_j^T into TMEM columns [t*128, t*128 + 128)
-            auto issue_s = [&](int t, int j) -> bool {
-                const int ks = j % KS;
-                if (!wait(&ctrl->k_full[ks], (j / KS) & 1)) return false;
+            // S_t = Q_t K^T of key tile gj (ring numbering) into TMEM columns [t*128, t*128 + 128)
+            auto issue_s = [&](int t, int gj) -> bool {
+                const int ks = gj % KS;
+                if (!wait(&ctrl->k_full[ks], (gj / KS) & 1)) return false;
                 ptx::tc_fence_after();
-                const uint32_t k_addr = ptx::smem_u32(smem + L::kKOff + ks * L::kKBytes);
-                const uint32_t qa = q_addr + t * L::kQBytes;
+                uint32_t k_addr = ptx::smem_u32(smem + L::kKOff + ks * L::kKBytes);
+                uint32_t qa = q_addr + t * L::kQBytes;
+                ptx::opaque(qa);  // rebuilt per call: the issuer keeps no descriptors live
+                // successive K-steps differ only in the start address (bits 0-13, 16-byte units;
+                // shared-memory addresses stay below 2^18, so the field never carries)
+                const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024), kd = ptx::sdesc_sw128(k_addr, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * kPanelBytes + (kk % 4) * 32;
-                    ptx::mma_ss(tmem + t * BQ, ptx::sdesc_sw128(qa + off, 16, 1024),
-                                ptx::sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
+                    ptx::mma_ss(tmem + t * BQ, qd + off, kd + off, kIdS, kk > 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(&ctrl->s_full[t]);
                 return true;
             };
-            bool ok = wait(&ctrl->q_full, 0);
-            if (ok && nA > 0) ok = issue_s(0, 0);
-            if (ok && nB > 0) ok = issue_s(1, 0);
-            if (ok) ptx::mma_commit(&ctrl->k_empty[0]);
-            for (int j = 0; ok && j < nmax; ++j) {
-                const int vs = j % VS;
-                for (int t = 0; ok && t < 2; ++t) {
-                    const int nt = t ? nB : nA;
-                    if (j >= nt) continue;
-                    if (!wait(&ctrl->p_full[t], j & 1) || !wait(&ctrl->v_full[vs], (j / VS) & 1)) {
+            // O_t += P_t V_j, then S_t(j+1) into the columns P_t(j) occupies: tcgen05.mma
+            // operations issued by one thread execute in issue order, so the product has read
+            // P_t(j) before S_t(j+1) is written; and the commit behind s_full[t] covers that
+            // product, so O_t is complete when the softmax sees S_t(j+1).
+            auto step = [&](int t, int nt, int ut, int j, int gj, int vs) -> bool {
+                if (!wait(&ctrl->p_full[t], (ut + j) & 1) || !wait(&ctrl->v_full[vs], (gj / VS) & 1))
+                    return false;
+                ptx::tc_fence_after();
+                const uint64_t vd = ptx::sdesc_sw128(ptx::smem_u32(smem + L::kVOff + vs * L::kVBytes),
+                                                     kPanelBytes, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    ptx::mma_ts(tmem + 2 * BQ + t * BQ, tmem + t * BQ + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                                kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == nt - 1) ptx::mma_commit(&ctrl->o_final[t]);
+                if (j + 1 < nt) {
+                    if (!issue_s(t, gj + 1)) return false;
+                    if (j + 2 == nt) ptx::mma_commit(&ctrl->q_empty[t]);  // last S_t has read Q_t
+                }
+                return true;
+            };
+            // first S of a tile: the previous item's last P V product of that tile, issued
+            // earlier, reads its P from these columns first (issue order)
+            auto first_s = [&](int t, int nt, int &nq, int g0) -> bool {
+                if (!wait(&ctrl->q_full[t], nq & 1) || !issue_s(t, g0)) return false;
+                ++nq;
+                if (nt == 1) ptx::mma_commit(&ctrl->q_empty[t]);
+                return true;
+            };
+            int g = 0, nqA = 0, nqB = 0, uA = 0, uB = 0;
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int k = item_index(r, cta, G);
+                if (k >= total) break;
+                const Item it = decode_item(a, k, false);
+                if (it.nmax == 0) continue;
+                const int nA = it.nA, nB = it.nB, nmax = it.nmax;
+                if (nA > 0 && !first_s(0, nA, nqA, g)) break;
+                if (nB > 0 && !first_s(1, nB, nqB, g)) break;
+                ptx::mma_commit(&ctrl->k_empty[g % KS]);
+                for (int j = 0; j < nmax; ++j) {
+                    const int gj = g + j, vs = gj % VS;
+                    if ((j < nA && !step(0, nA, uA, j, gj, vs)) || (j < nB && !step(1, nB, uB, j, gj, vs))) {
                         ok = false;
                         break;
                     }
-                    ptx::tc_fence_after();
-                    const uint32_t v_addr = ptx::smem_u32(smem + L::kVOff + vs * L::kVBytes);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_ts(tmem + 2 * BQ + t * BQ, tmem + t * BQ + kk * 8,
-                                    ptx::sdesc_sw128(v_addr + kk * 16 * 128, kPanelBytes, 1024), kIdO,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    if (j == nt - 1) ptx::mma_commit(&ctrl->o_final[t]);
-                    // S_t(j+1) overwrites the columns P_t(j) occupies: tcgen05.mma operations
-                    // issued by one thread execute in issue order, so the product just issued
-                    // has read P_t(j) before S_t(j+1) is written; and the commit behind
-                    // s_full[t] covers that product, so O_t is complete when the softmax sees
-                    // S_t(j+1).
-                    if (j + 1 < nt && !issue_s(t, j + 1)) {
-                        ok = false;
-                        break;
+                    // the last V slot of the item is released by tile B's epilogue, which stages
+                    // its output there
+                    if (j + 1 < nmax) {
+                        ptx::mma_commit(&ctrl->v_empty[vs]);
+                        ptx::mma_commit(&ctrl->k_empty[(gj + 1) % KS]);
                     }
                 }
-                if (!ok) break;
-                ptx::mma_commit(&ctrl->v_empty[vs]);
-                if (j + 1 < nmax) ptx::mma_commit(&ctrl->k_empty[(j + 1) % KS]);
+                g += nmax;
+                uA += nA;
+                uB += nB;
             }
             ptx::mma_commit(&ctrl->final_mma);
             if (!ptx::mbar_wait_quiet(&ctrl->final_mma, 0, kWaitLimitNs)) atomicOr(a.flags, kFlagWaitTimeout);
@@ -247,37 +314,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::regs_inc<kRegsSoftmax>();
         // ------------------------------------------------------------ softmax warpgroups
+        const int X = (warp >= 8) ? 1 : 0;              // query tile of this warpgroup
+        const int r = (int)threadIdx.x - 128 - X * BQ;  // row in the tile == TMEM lane
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t s_col = X * BQ, o_col = 2 * BQ + X * BQ;
-        const int r0 = q0 + X * BQ;
         const float c = a.scale_log2;
-        const float *bias_row = nullptr;
-        if (kBias && i < a.Nq) bias_row = a.bias + b * a.bs0 + h * a.bs1 + (long long)i * a.bs2;
-        const bool bias_vec = (reinterpret_cast<uintptr_t>(bias_row) & 15u) == 0;
-        __nv_bfloat16 *orow = (i < a.Nq) ? a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2 : nullptr;
-        float *lse_out = (a.lse && i < a.Nq) ? a.lse + ((long long)b * a.H + h) * a.Nq + i : nullptr;
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) -> bool {
             const bool w = ptx::mbar_wait(bar, parity, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
             return __all_sync(0xffffffffu, w);
         };
-        if (nX == 0) {
-            if (orow) write_empty_row<DV>(orow, lse_out);
-        } else {
+        int g = 0, u = 0, nfin = 0;
+        bool ok = true;
+        for (int rr = 0; ok; ++rr) {
+            const int k = item_index(rr, cta, G);
+            if (k >= total) break;
+            const Item it = decode_item(a, k, threadIdx.x == 128);
+            const int nX = X ? it.nB : it.nA;
+            const int r0 = it.q0 + X * BQ, i = r0 + r;
+            // this row's output and log-sum-exp (null past Nq)
+            auto out_row = [&]() -> __nv_bfloat16 * {
+                return (i < a.Nq) ? a.o + it.b * a.os0 + (long long)i * a.os1 + it.h * a.os2 : nullptr;
+            };
+            auto out_lse = [&]() -> float * {
+                return (a.lse && i < a.Nq) ? a.lse + ((long long)it.b * a.H + it.h) * a.Nq + i : nullptr;
+            };
+            if (nX == 0) {  // no key visible to any row of this tile
+                if (i < a.Nq) write_empty_row<DV>(out_row(), out_lse());
+                g += it.nmax;
+                continue;
+            }
+            const int shift = it.n - a.Nq;
+            const float *bias_row = nullptr;
+            if (kBias && i < a.Nq) bias_row = a.bias + it.b * a.bs0 + it.h * a.bs1 + (long long)i * a.bs2;
+            const bool bias_vec = (reinterpret_cast<uintptr_t>(bias_row) & 15u) == 0;
+            const int lim = a.causal ? min(it.n, i + shift + 1) : it.n;  // keys < lim are visible
             float m_run = -INFINITY, l_run = 0.f;
-            bool ok = true;
-            const int lim = a.causal ? min(n, i + shift + 1) : n;  // keys < lim are visible
             float x[BK];  // with a bias: the next tile's bias, loaded ahead
-            if (kBias) load_bias(bias_row, bias_vec, 0, n, x);
+            if (kBias) load_bias(bias_row, bias_vec, 0, it.n, x);
             for (int j = 0; j < nX; ++j) {
-                const int kv0 = j * BK;
-                if (!wait_warp(&ctrl->s_full[X], j & 1)) {
+                const int kv0 = j * BK, gj = g + j;
+                if (!wait_warp(&ctrl->s_full[X], (u + j) & 1)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 if (kBias) load_s_row_bias(lane_addr + s_col, c, x);
                 else load_s_row(lane_addr + s_col, x);
-                const bool need_mask = (kv0 + BK > n) || (a.causal && kv0 + BK - 1 > r0 + shift);
+                const bool need_mask = (kv0 + BK > it.n) || (a.causal && kv0 + BK - 1 > r0 + shift);
                 const float mt = tile_logits<kBias>(x, c, kv0, need_mask, lim);
                 bool rescale;
                 const float alpha = update_max(mt, m_run, rescale);
@@ -285,44 +368,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_run = fmaf(alpha, l_run, lsum);
                 if (__any_sync(0xffffffffu, rescale)) scale_o<DV>(lane_addr + o_col, alpha);
                 // value rows past n inside this tile may hold anything: the warpgroup of the
-                // first tile that uses V_j zeroes them before its product reads V_j
-                if (kv0 + BK > n && n < a.Nk && (X == 0 || j >= nA)) {
-                    if (!wait_warp(&ctrl->v_full[j % VS], (j / VS) & 1)) {
+                // first query tile that uses V_j zeroes them before its product reads V_j
+                if (kv0 + BK > it.n && it.n < a.Nk && (X == 0 || j >= it.nA)) {
+                    if (!wait_warp(&ctrl->v_full[gj % VS], (gj / VS) & 1)) {
                         ok = false;
                         break;
                     }
-                    if (kv0 + r >= n && kv0 + r < a.Nk)
-                        zero_v_row<DV>(smem + L::kVOff + (j % VS) * L::kVBytes, r);
+                    if (kv0 + r >= it.n && kv0 + r < a.Nk)
+                        zero_v_row<DV>(smem + L::kVOff + (gj % VS) * L::kVBytes, r);
                     ptx::fence_proxy_async_smem();
                 }
                 store_p(lane_addr + s_col, x);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&ctrl->p_full[X]);
-                if (kBias && j + 1 < nX) load_bias(bias_row, bias_vec, kv0 + BK, n, x);
+                if (kBias && j + 1 < nX) load_bias(bias_row, bias_vec, kv0 + BK, it.n, x);
             }
-            if (ok && wait_warp(&ctrl->o_final[X], 0)) {
-                ptx::tc_fence_after();
-                if constexpr (DV <= DK) {
-                    // divide once, stage the bf16 tile in Q_X's shared memory (its last reader,
-                    // S_X of the last key tile, completed before o_final) and store it with TMA
-                    uint8_t *stage = smem + X * L::kQBytes;
-                    stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, lse_out);
-                    ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&ctrl->o_staged[X]);
-                    // one thread stores the tile once all 128 rows are staged (a bounded wait:
-                    // a warp that gave up earlier never arrives, and the store is then skipped)
-                    if (r == 0 && ptx::mbar_wait(&ctrl->o_staged[X], 0, abort, a.flags,
-                                                 kFlagWaitTimeout, kWaitLimitNs)) {
+            if (!ok || !wait_warp(&ctrl->o_final[X], nfin & 1)) break;
+            ptx::tc_fence_after();
+            // divide once and store the row; the next item's first P V product overwrites O_X
+            // only after this thread's next P hand-off, which follows these TMEM loads
+            // Each tile's rows go through shared memory in the swizzled box layout, and one
+            // thread stores the tile with TMA.  Tile A stages in its Q buffer (its last S
+            // product has completed), which the store then releases to the producer.  Tile B
+            // finishes last (it sees at least as many key tiles as tile A) and stages in the
+            // item's last V slot, whose products have all completed, so that the next item's
+            // Q_B can load meanwhile; the store releases that slot.  With dv > dk the Q buffer
+            // is too small and tile A writes its rows directly.
+            if (!kStageA && X == 0) {
+                write_row<DV>(lane_addr + o_col, l_run, m_run, out_row(), out_lse());
+                ptx::tc_fence_before();
+            } else {
+                const int sl = (g + it.nmax - 1) % VS;
+                uint8_t *stage = X ? smem + L::kVOff + sl * L::kVBytes : smem;
+                stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, out_lse());
+                ptx::tc_fence_before();
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&ctrl->o_staged[X]);
+                if (r == 0) {
+                    if (ptx::mbar_wait(&ctrl->o_staged[X], nfin & 1, abort, a.flags, kFlagWaitTimeout,
+                                       kWaitLimitNs)) {
 #pragma unroll
                         for (int p = 0; p < DV / 64; ++p)
-                            ptx::tma_store_4d(&tm_o, stage + p * kPanelBytes, p * 64, r0, h, b);
+                            ptx::tma_store_4d(&tm_o, stage + p * kPanelBytes, p * 64, r0, it.h, it.b);
                         ptx::bulk_commit();
                         ptx::bulk_wait_read();
                     }
-                } else {
-                    write_row<DV>(lane_addr + o_col, l_run, m_run, orow, lse_out);
+                    ptx::mbar_arrive(X ? &ctrl->v_empty[sl] : &ctrl->q_empty[0]);
                 }
             }
+            g += it.nmax;
+            u += nX;
+            ++nfin;
         }
     }
 
@@ -342,9 +438,13 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     auto kern = fwd_bf16_pair_kernel<DK, DV, kBias>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    const long long grid = (long long)a.n_items * a.B * a.H;
-    if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, mo, a);
+    const long long total = (long long)a.n_items * a.B * a.H;
+    if (total > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
+    // persistent: one CTA per SM (each holds most of the shared memory and all of TMEM)
+    const int sms = sm_count();
+    if (sms <= 0) return fail(ATTN_ERR_CUDA, "could not read the SM count");
+    const unsigned grid = (unsigned)(total < sms ? total : sms);
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16_pair launch: %s", cudaGetErrorString(e));
     return ATTN_OK;

@@ -236,6 +236,10 @@ __device__ __forceinline__ void regs_inc() {
 
 // ------------------------------------------------------------------ descriptors
 
+// Hides a value from the optimiser, so that what is derived from it is recomputed where it
+// is used instead of being hoisted and kept live in registers.
+__device__ __forceinline__ void opaque(uint32_t &v) { asm volatile("" : "+r"(v)); }
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and stride byte
 // offsets (all >> 4), version 1 at bits 46-47, swizzle mode at bits 61-63
 // (2 = 128-byte swizzle).  Matrices start on 1024-byte boundaries (base offset 0).
