@@ -98,6 +98,16 @@ __device__ __forceinline__ int item_index(int r, int c, int G) {
     return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
+// The first item after the r-th of CTA c that has a key tile (nmax = 0 if none is left).
+__device__ __forceinline__ Item next_item(const Args &a, int r, int c, int G, int total) {
+    for (int k = item_index(++r, c, G); k < total; k = item_index(++r, c, G)) {
+        const Item it = decode_item(a, k, false);
+        if (it.nmax > 0) return it;
+    }
+    Item none{};
+    return none;
+}
+
 template <int DK, int DV, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -117,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = a.B * a.H * a.n_items;
     const int G = (int)gridDim.x, cta = (int)blockIdx.x;
 
+    bool pre_q = false, pre_k = false;  // loads thread 0 issued ahead of the block barrier
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(&ctrl->q_full[t], 1);
@@ -139,12 +150,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&ctrl->final_mma, 1);
         ctrl->abort = 0;
         ptx::fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
         ptx::prefetch_tmap(&tm_o);
+        // this thread is the producer: the first item's Q_A and K_0 start loading before the
+        // tensor-memory allocation and the block barrier
+        const Item it = next_item(a, -1, cta, G, total);
+        if (it.nmax > 0) {
+            if (it.nA > 0) {
+                ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], L::kQBytes);
+#pragma unroll
+                for (int p = 0; p < DK / 64; ++p)
+                    ptx::tma_load_4d(smem + p * kPanelBytes, &tm_q, &ctrl->q_full[0], p * 64, it.q0, it.h,
+                                     it.b);
+                pre_q = true;
+            }
+            ptx::mbar_arrive_expect_tx(&ctrl->k_full[0], L::kKBytes);
+#pragma unroll
+            for (int p = 0; p < DK / 64; ++p)
+                ptx::tma_load_4d(smem + L::kKOff + p * kPanelBytes, &tm_k, &ctrl->k_full[0], p * 64, 0, it.h,
+                                 it.b);
+            pre_k = true;
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(&ctrl->tmem_base, kTmemCols);
@@ -162,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int g = 0, nqA = 0, nqB = 0, last_k = -1, last_v = -1;
+            int g = 0, nqA = pre_q ? 1 : 0, nqB = 0, last_k = pre_k ? 0 : -1, last_v = -1;
             // Q_t of the next item, once the previous item's last S_t has read the buffer
             auto load_q = [&](int t, int &nq, const Item &it) -> bool {
                 if (nq > 0 && !ptx::mbar_wait(&ctrl->q_empty[t], (nq - 1) & 1, abort, a.flags,
@@ -182,22 +210,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k >= total) break;
                 const Item it = decode_item(a, k, false);
                 if (it.nmax == 0) continue;
-                if (it.nA > 0 && !load_q(0, nqA, it)) break;
-                if (it.nB > 0 && !load_q(1, nqB, it)) break;
+                // Q_A, K_0, Q_B, V_0, K_1, ...: S_A(0) needs only the first two
+                if (it.nA > 0 && !(g == 0 && pre_q) && !load_q(0, nqA, it)) break;
                 for (int j = 0; ok && j < it.nmax; ++j) {
                     const int gj = g + j, ks = gj % KS, vs = gj % VS;
-                    if (gj >= KS && !ptx::mbar_wait(&ctrl->k_empty[ks], ((gj / KS) - 1) & 1, abort,
-                                                    a.flags, kFlagWaitTimeout, kWaitLimitNs)) {
+                    if (!(gj == 0 && pre_k)) {
+                        if (gj >= KS && !ptx::mbar_wait(&ctrl->k_empty[ks], ((gj / KS) - 1) & 1, abort,
+                                                        a.flags, kFlagWaitTimeout, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *sK = smem + L::kKOff + ks * L::kKBytes;
+                        ptx::mbar_arrive_expect_tx(&ctrl->k_full[ks], L::kKBytes);
+#pragma unroll
+                        for (int p = 0; p < DK / 64; ++p)
+                            ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[ks], p * 64, j * BK,
+                                             it.h, it.b);
+                        last_k = gj;
+                    }
+                    if (j == 0 && it.nB > 0 && !load_q(1, nqB, it)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *sK = smem + L::kKOff + ks * L::kKBytes;
-                    ptx::mbar_arrive_expect_tx(&ctrl->k_full[ks], L::kKBytes);
-#pragma unroll
-                    for (int p = 0; p < DK / 64; ++p)
-                        ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[ks], p * 64, j * BK,
-                                         it.h, it.b);
-                    last_k = gj;
                     if (gj >= VS && !ptx::mbar_wait(&ctrl->v_empty[vs], ((gj / VS) - 1) & 1, abort,
                                                     a.flags, kFlagWaitTimeout, kWaitLimitNs)) {
                         ok = false;
