@@ -97,21 +97,18 @@ __device__ __forceinline__ void load_bias(const float *bias_row, bool bias_vec, 
     }
 }
 
-// Row r of a bias tile staged in shared memory by TMA (four 32-key panels of 128 rows x 128
-// bytes, 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)), in base-2 units,
-// into xb.  Eight consecutive rows read eight different bank groups.
-__device__ __forceinline__ void read_bias_stage(const uint8_t *stage, int r, float (&xb)[BK]) {
+// Row r of a 32-key bias panel staged in shared memory by TMA (128 rows x 128 bytes, 128-byte
+// swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)), in base-2 units, into keys
+// [32 p, 32 p + 32) of xb.  Eight consecutive rows read eight different bank groups.
+__device__ __forceinline__ void read_bias_panel(const uint8_t *panel, int r, int p, float (&xb)[BK]) {
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float4 v = *reinterpret_cast<const float4 *>(stage + p * kPanelBytes + r * 128 +
-                                                               ((c ^ (r & 7)) * 16));
-            xb[p * 32 + 4 * c + 0] = v.x * kLog2e;
-            xb[p * 32 + 4 * c + 1] = v.y * kLog2e;
-            xb[p * 32 + 4 * c + 2] = v.z * kLog2e;
-            xb[p * 32 + 4 * c + 3] = v.w * kLog2e;
-        }
+    for (int c = 0; c < 8; ++c) {
+        const float4 v = *reinterpret_cast<const float4 *>(panel + r * 128 + ((c ^ (r & 7)) * 16));
+        xb[p * 32 + 4 * c + 0] = v.x * kLog2e;
+        xb[p * 32 + 4 * c + 1] = v.y * kLog2e;
+        xb[p * 32 + 4 * c + 2] = v.z * kLog2e;
+        xb[p * 32 + 4 * c + 3] = v.w * kLog2e;
+    }
 }
 
 // x = S * c + xb in place: the row of S from TMEM columns [taddr, taddr + BK), 32 columns at a

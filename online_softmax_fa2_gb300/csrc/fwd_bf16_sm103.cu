@@ -57,21 +57,25 @@ constexpr int kSBufs = 3;          // S/P buffers: TMEM columns [0,128), [128,25
 constexpr uint32_t kTmemO = 384;   // O accumulator columns [384, 384 + dv)
 constexpr int kMaxStages = 4;
 
+// kTmaBias: the bias streams through shared memory as 32-key panels (128 rows x 32 keys fp32,
+// 128-byte swizzled), four per key tile, in a ring of four filled by a producer of its own:
+// a panel is refilled as soon as the softmax has read it.
+constexpr int kBiasPanels = 4;
+constexpr int kBiasBytes = kBiasPanels * kPanelBytes;
+
 struct Ctrl {
     uint64_t q_full;
     uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
     uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
     uint64_t o_done;     // one completion per P V product (O rescale waits on PV_{j-1})
     uint64_t o_final;    // completes once, after the last P V product
-    uint64_t b_full, b_empty;  // bias tile staged by TMA (bias kernels with a TMA-able bias)
+    uint64_t o_staged;   // every row of the output tile written to its shared-memory stage
+    uint64_t b_full[kBiasPanels], b_empty[kBiasPanels];  // the bias panel ring
     uint64_t final_mma;
     uint32_t tmem_base;
     int abort;
 };
 
-// kTmaBias: the bias tile (128 rows x 128 keys fp32, four 32-key panels, 128-byte swizzled)
-// is staged in shared memory by TMA; one K and one V stage then make room for it.
-constexpr int kBiasBytes = 4 * kPanelBytes;
 
 template <int DK, int DV, bool kTmaBias = false>
 struct Layout {
@@ -79,14 +83,15 @@ struct Layout {
     static constexpr int kKBytes = (DK / 64) * kPanelBytes;
     static constexpr int kVBytes = (DV / 64) * kPanelBytes;
     static constexpr int kFixed = kQBytes + (kTmaBias ? kBiasBytes : 0) + 2048;
-    // deepest equal K and V rings that fit next to Q (and the bias tile)
-    static constexpr int kStages =
-        (kFixed + 4 * (kKBytes + kVBytes) <= kSmemMax) ? 4
-        : (kFixed + 3 * (kKBytes + kVBytes) <= kSmemMax) ? 3
-        : (kFixed + 2 * (kKBytes + kVBytes) <= kSmemMax) ? 2 : 1;
+    static constexpr bool fits(int ks, int vs) { return kFixed + ks * kKBytes + vs * kVBytes <= kSmemMax; }
+    // the deepest K and V rings that fit next to Q (and the bias panels); a V tile waits for
+    // the P V product two tiles back, so V gets the second stage first
+    static constexpr int kKStages = fits(4, 4) ? 4 : fits(3, 3) ? 3 : fits(2, 3) ? 2 : fits(2, 2) ? 2 : 1;
+    static constexpr int kVStages = fits(4, 4) ? 4 : fits(3, 3) ? 3 : fits(2, 3) ? 3 : fits(2, 2) ? 2
+                                  : fits(1, 2) ? 2 : 1;
     static constexpr int kKOff = kQBytes;                       // K ring
-    static constexpr int kVOff = kQBytes + kStages * kKBytes;   // V ring
-    static constexpr int kBOff = kVOff + kStages * kVBytes;     // bias tile
+    static constexpr int kVOff = kQBytes + kKStages * kKBytes;  // V ring
+    static constexpr int kBOff = kVOff + kVStages * kVBytes;    // bias panels
     static constexpr int kDataBytes = kBOff + (kTmaBias ? kBiasBytes : 0);
     static constexpr int kBytes = kDataBytes + (int)sizeof(Ctrl) + 1024;  // + alignment slack
     static_assert(kBytes <= kSmemMax, "shared memory budget");
@@ -96,10 +101,10 @@ template <int DK, int DV, bool kBias, bool kTmaBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_b,
-                    const Args a) {
+                    const __grid_constant__ CUtensorMap tm_o, const Args a) {
     static_assert(kBias || !kTmaBias, "a staged bias needs a bias");
     using L = Layout<DK, DV, kTmaBias>;
-    constexpr int kStages = L::kStages;
+    constexpr int KS = L::kKStages, VS = L::kVStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -129,9 +134,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&ctrl->q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < KS; ++s) {
             ptx::mbar_init(&ctrl->k_full[s], 1);
             ptx::mbar_init(&ctrl->k_empty[s], 1);
+        }
+        for (int s = 0; s < VS; ++s) {
             ptx::mbar_init(&ctrl->v_full[s], 1);
             ptx::mbar_init(&ctrl->v_empty[s], 1);
         }
@@ -142,17 +149,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(&ctrl->o_done, 1);
         ptx::mbar_init(&ctrl->o_final, 1);
-        ptx::mbar_init(&ctrl->b_full, 1);
-        ptx::mbar_init(&ctrl->b_empty, 128);
+        ptx::mbar_init(&ctrl->o_staged, 128);
+        for (int s = 0; s < kBiasPanels; ++s) {
+            ptx::mbar_init(&ctrl->b_full[s], 1);
+            ptx::mbar_init(&ctrl->b_empty[s], 128);
+        }
         ptx::mbar_init(&ctrl->final_mma, 1);
         ctrl->abort = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (threadIdx.x == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_o);
         if (kTmaBias) ptx::prefetch_tmap(&tm_b);
+        // this thread produces Q and K: both start loading before the tensor-memory
+        // allocation and the block barrier
+        ptx::mbar_arrive_expect_tx(&ctrl->q_full, L::kQBytes);
+#pragma unroll
+        for (int p = 0; p < DK / 64; ++p)
+            ptx::tma_load_4d(sQ + p * kPanelBytes, &tm_q, &ctrl->q_full, p * 64, q0, h, b);
+        ptx::mbar_arrive_expect_tx(&ctrl->k_full[0], L::kKBytes);
+#pragma unroll
+        for (int p = 0; p < DK / 64; ++p)
+            ptx::tma_load_4d(smem + L::kKOff + p * kPanelBytes, &tm_k, &ctrl->k_full[0], p * 64, 0, h, b);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&ctrl->tmem_base, kTmemCols);
@@ -164,57 +185,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = ctrl->tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer: Q, K
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(&ctrl->q_full, L::kQBytes);
-#pragma unroll
-            for (int p = 0; p < DK / 64; ++p)
-                ptx::tma_load_4d(sQ + p * kPanelBytes, &tm_q, &ctrl->q_full, p * 64, q0, h, b);
-            int last_k = -1, last_v = -1, last_b = -1;  // last tiles whose copies were issued
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages &&
-                    !ptx::mbar_wait(&ctrl->k_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
-                                    kFlagWaitTimeout, kWaitLimitNs))
+            int last_k = 0;  // last tile whose copy was issued (Q and K_0: issued above)
+            for (int j = 1; j < n_tiles; ++j) {
+                const int st = j % KS;
+                if (j >= KS && !ptx::mbar_wait(&ctrl->k_empty[st], ((j / KS) - 1) & 1, abort, a.flags,
+                                               kFlagWaitTimeout, kWaitLimitNs))
                     break;
                 uint8_t *sK = smem + L::kKOff + st * L::kKBytes;
-                uint8_t *sV = smem + L::kVOff + st * L::kVBytes;
                 ptx::mbar_arrive_expect_tx(&ctrl->k_full[st], L::kKBytes);
 #pragma unroll
                 for (int p = 0; p < DK / 64; ++p)
                     ptx::tma_load_4d(sK + p * kPanelBytes, &tm_k, &ctrl->k_full[st], p * 64, j * BK, h, b);
                 last_k = j;
-                if (kTmaBias) {
-                    // bias tile j, as soon as the softmax has read tile j-1 (ahead of V_j, which
-                    // waits for the previous P V product)
-                    if (j >= 1 && !ptx::mbar_wait(&ctrl->b_empty, (j - 1) & 1, abort, a.flags,
-                                                  kFlagWaitTimeout, kWaitLimitNs))
-                        break;
-                    ptx::mbar_arrive_expect_tx(&ctrl->b_full, kBiasBytes);
-#pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        ptx::tma_load_4d(smem + L::kBOff + p * kPanelBytes, &tm_b, &ctrl->b_full,
-                                         j * BK + 32 * p, q0, h, b);
-                    last_b = j;
-                }
-                if (j >= kStages &&
-                    !ptx::mbar_wait(&ctrl->v_empty[st], ((j / kStages) - 1) & 1, abort, a.flags,
-                                    kFlagWaitTimeout, kWaitLimitNs))
+            }
+            if (*abort) {  // let copies still in flight land before the CTA exits
+                ptx::mbar_wait_quiet(&ctrl->q_full, 0, kWaitLimitNs);
+                for (int j = max(0, last_k - KS + 1); j <= last_k; ++j)
+                    ptx::mbar_wait_quiet(&ctrl->k_full[j % KS], (j / KS) & 1, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ TMA producer: V
+        // (a thread of its own, so that a V tile waiting for its slot never holds up K)
+        if (lane == 0) {
+            int last_v = -1;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % VS;
+                if (j >= VS && !ptx::mbar_wait(&ctrl->v_empty[st], ((j / VS) - 1) & 1, abort, a.flags,
+                                               kFlagWaitTimeout, kWaitLimitNs))
                     break;
+                uint8_t *sV = smem + L::kVOff + st * L::kVBytes;
                 ptx::mbar_arrive_expect_tx(&ctrl->v_full[st], L::kVBytes);
 #pragma unroll
                 for (int p = 0; p < DV / 64; ++p)
                     ptx::tma_load_4d(sV + p * kPanelBytes, &tm_v, &ctrl->v_full[st], p * 64, j * BK, h, b);
                 last_v = j;
             }
-            if (*abort) {  // let copies still in flight land before the CTA exits
-                ptx::mbar_wait_quiet(&ctrl->q_full, 0, kWaitLimitNs);
-                for (int j = max(0, last_k - kStages + 1); j <= last_k; ++j)
-                    ptx::mbar_wait_quiet(&ctrl->k_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
-                for (int j = max(0, last_v - kStages + 1); j <= last_v; ++j)
-                    ptx::mbar_wait_quiet(&ctrl->v_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
-                if (last_b >= 0) ptx::mbar_wait_quiet(&ctrl->b_full, last_b & 1, kWaitLimitNs);
-            }
+            if (*abort)
+                for (int j = max(0, last_v - VS + 1); j <= last_v; ++j)
+                    ptx::mbar_wait_quiet(&ctrl->v_full[j % VS], (j / VS) & 1, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ tensor-core issuer
@@ -224,13 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_addr = ptx::smem_u32(sQ);
             bool ok = ptx::mbar_wait(&ctrl->q_full, 0, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
             auto issue_s = [&](int j) -> bool {
-                const int st = j % kStages, buf = j % kSBufs;
+                const int st = j % KS, buf = j % kSBufs;
                 // buffer reuse: the P V product of tile j - 3 (which read this buffer) is done
                 if (j >= kSBufs &&
                     !ptx::mbar_wait(&ctrl->pv_done[buf], ((j / kSBufs) - 1) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
                     return false;
-                if (!ptx::mbar_wait(&ctrl->k_full[st], (j / kStages) & 1, abort, a.flags,
+                if (!ptx::mbar_wait(&ctrl->k_full[st], (j / KS) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
                     return false;
                 ptx::tc_fence_after();
@@ -248,11 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ok = issue_s(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-                const int st = j % kStages, buf = j % kSBufs;
+                const int st = j % VS, buf = j % kSBufs;
                 if (!ptx::mbar_wait(&ctrl->p_full[buf], (j / kSBufs) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
                     break;
-                if (!ptx::mbar_wait(&ctrl->v_full[st], (j / kStages) & 1, abort, a.flags,
+                if (!ptx::mbar_wait(&ctrl->v_full[st], (j / VS) & 1, abort, a.flags,
                                     kFlagWaitTimeout, kWaitLimitNs))
                     break;
                 ptx::tc_fence_after();
@@ -274,6 +285,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             // all tensor-core work of this CTA done before TMEM is released
             ptx::mma_commit(&ctrl->final_mma);
             if (!ptx::mbar_wait_quiet(&ctrl->final_mma, 0, kWaitLimitNs)) atomicOr(a.flags, kFlagWaitTimeout);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ bias producer
+        if (kTmaBias && lane == 0) {
+            // panel q of the key tiles (32 keys each, four per tile) into ring slot q % 6, as
+            // soon as the softmax has read what the slot held
+            const int n_panels = 4 * n_tiles;
+            int last = -1;
+            for (int q = 0; q < n_panels; ++q) {
+                const int sl = q % kBiasPanels;
+                if (q >= kBiasPanels && !ptx::mbar_wait(&ctrl->b_empty[sl], ((q / kBiasPanels) - 1) & 1, abort,
+                                                        a.flags, kFlagWaitTimeout, kWaitLimitNs))
+                    break;
+                ptx::mbar_arrive_expect_tx(&ctrl->b_full[sl], kPanelBytes);
+                ptx::tma_load_4d(smem + L::kBOff + sl * kPanelBytes, &tm_b, &ctrl->b_full[sl],
+                                 (q >> 2) * BK + 32 * (q & 3), q0, h, b);
+                last = q;
+            }
+            if (*abort)  // let copies still in flight land before the CTA exits
+                for (int q = max(0, last - kBiasPanels + 1); q <= last; ++q)
+                    ptx::mbar_wait_quiet(&ctrl->b_full[q % kBiasPanels], (q / kBiasPanels) & 1, kWaitLimitNs);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroup
@@ -297,13 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kBias && !kTmaBias) load_bias(bias_row, bias_vec, 0, n, x);
         for (int j = 0; j < n_tiles; ++j) {
             const int buf = j % kSBufs, kv0 = j * BK;
-            if (kTmaBias) {  // this tile's bias row from the staged tile, then free the stage
-                if (!wait_warp(&ctrl->b_full, j & 1)) {
-                    ok = false;
-                    break;
+            if (kTmaBias) {  // this tile's bias row from its four staged panels, freeing each
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int q = 4 * j + p, sl = q % kBiasPanels;
+                    if (!wait_warp(&ctrl->b_full[sl], (q / kBiasPanels) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    read_bias_panel(smem + L::kBOff + sl * kPanelBytes, r, p, x);
+                    ptx::mbar_arrive(&ctrl->b_empty[sl]);
                 }
-                read_bias_stage(smem + L::kBOff, r, x);
-                ptx::mbar_arrive(&ctrl->b_empty);
+                if (!ok) break;
             }
             if (!wait_warp(&ctrl->s_full[buf], (j / kSBufs) & 1)) {
                 ok = false;
@@ -334,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // value rows past n inside this tile (still in bounds) may hold anything: zero them
             if (kv0 + BK > n && n < a.Nk) {
-                const int st = j % kStages;
-                if (!wait_warp(&ctrl->v_full[st], (j / kStages) & 1)) {
+                const int st = j % VS;
+                if (!wait_warp(&ctrl->v_full[st], (j / VS) & 1)) {
                     ok = false;
                     break;
                 }
@@ -350,12 +387,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kBias && !kTmaBias && j + 1 < n_tiles) load_bias(bias_row, bias_vec, kv0 + BK, n, x);
         }
 
-        // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf
+        // epilogue: o = u / l once, lse = m + ln l; empty rows o = +0.0, lse = -inf.  The rows
+        // go into Q's shared memory (its last reader, the last S product, completed before
+        // o_final) in the swizzled box layout, and one thread stores the tile with TMA (rows
+        // past Nq are not written) once every row is staged
         if (ok && wait_warp(&ctrl->o_final, 0)) {
             ptx::tc_fence_after();
-            write_row<DV>(lane_addr + kTmemO, l_run, m_run,
-                          (i < a.Nq) ? a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2 : nullptr,
+            stage_row<DV>(lane_addr + kTmemO, l_run, m_run, sQ, r,
                           (a.lse && i < a.Nq) ? a.lse + ((long long)b * a.H + h) * a.Nq + i : nullptr);
+            ptx::tc_fence_before();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&ctrl->o_staged);
+            if (r == 0 && ptx::mbar_wait(&ctrl->o_staged, 0, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs)) {
+#pragma unroll
+                for (int p = 0; p < DV / 64; ++p) ptx::tma_store_4d(&tm_o, sQ + p * kPanelBytes, p * 64, q0, h, b);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read();
+            }
         }
     }
 
@@ -427,13 +475,14 @@ bool encode_bias(CUtensorMap *m, const attn_fwd_params_t &p) {
 
 template <int DK, int DV, bool kBias, bool kTmaBias>
 attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                       const CUtensorMap &mb, const Args &a, unsigned grid, cudaStream_t s) {
+                       const CUtensorMap &mb, const CUtensorMap &mo, const Args &a, unsigned grid,
+                       cudaStream_t s) {
     int smem = Layout<DK, DV, kTmaBias>::kBytes;
     if (smem < 116 * 1024) smem = 116 * 1024;  // one CTA per SM: it owns all 512 TMEM columns
     auto kern = fwd_bf16_kernel<DK, DV, kBias, kTmaBias>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mb, a);
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mb, mo, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16 launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
@@ -441,9 +490,10 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 
 template <bool kBias, bool kTmaBias>
 attn_status_t dispatch(int dk, int dv, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                       const CUtensorMap &mb, const Args &a, unsigned grid, cudaStream_t s) {
-    if (dk == 192 && dv == 128) return launch_t<192, 128, kBias, kTmaBias>(mq, mk, mv, mb, a, grid, s);
-    if (dk == 192 && dv == 64) return launch_t<192, 64, kBias, kTmaBias>(mq, mk, mv, mb, a, grid, s);
+                       const CUtensorMap &mb, const CUtensorMap &mo, const Args &a, unsigned grid,
+                       cudaStream_t s) {
+    if (dk == 192 && dv == 128) return launch_t<192, 128, kBias, kTmaBias>(mq, mk, mv, mb, mo, a, grid, s);
+    if (dk == 192 && dv == 64) return launch_t<192, 64, kBias, kTmaBias>(mq, mk, mv, mb, mo, a, grid, s);
     return fail(ATTN_ERR_UNSUPPORTED, "no one-tile bf16 kernel for dk=%d dv=%d", dk, dv);
 }
 
@@ -478,18 +528,16 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     a.kv_lens = p.kv_lens;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
-    if (pair) {
-        CUtensorMap mo;
-        if ((st = encode(&mo, p.o, p.B, p.Nq, p.H, p.dv, p.o_stride, "o"))) return st;
-        return launch_fwd_bf16_pair(mq, mk, mv, mo, a, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
-    }
+    CUtensorMap mo;
+    if ((st = encode(&mo, p.o, p.B, p.Nq, p.H, p.dv, p.o_stride, "o"))) return st;
+    if (pair) return launch_fwd_bf16_pair(mq, mk, mv, mo, a, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
     const long long grid = (long long)a.n_items * p.B * p.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
     CUtensorMap mb = mq;  // read only by kernels that stage the bias
     if (p.bias && p.Nk > 0 && encode_bias(&mb, p))
-        return dispatch<true, true>((int)p.dk, (int)p.dv, mq, mk, mv, mb, a, (unsigned)grid, s);
-    if (p.bias) return dispatch<true, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, a, (unsigned)grid, s);
-    return dispatch<false, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, a, (unsigned)grid, s);
+        return dispatch<true, true>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
+    if (p.bias) return dispatch<true, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
+    return dispatch<false, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
 }
 
 }  // namespace attn
