@@ -97,6 +97,22 @@ struct Layout {
     static_assert(kBytes <= kSmemMax, "shared memory budget");
 };
 
+// With per-sequence key lengths the work of a query tile depends on its sequence, so for up to
+// 32 sequences the CTAs take the sequences in order of decreasing length (ties by index), the
+// longest work first.  Warp-collective: lane t holds sequence t's length, counts the lanes
+// ahead of it, and the sequence of rank R is the lane whose count is R.
+__device__ __forceinline__ int batch_by_rank(const Args &a, int R) {
+    const int lane = threadIdx.x & 31;
+    const int len = lane < a.B ? seq_len(a, lane, false) : -1;
+    int rank = 0;
+#pragma unroll
+    for (int o = 0; o < 32; ++o) {
+        const int lo = __shfl_sync(0xffffffffu, len, o);
+        rank += (lo > len) || (lo == len && o < lane);
+    }
+    return __ffs(__ballot_sync(0xffffffffu, lane < a.B && rank == R)) - 1;
+}
+
 template <int DK, int DV, bool kBias, bool kTmaBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -113,9 +129,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort = &ctrl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bhn = a.B * a.H;
-    const int qt = a.n_items - 1 - (int)(blockIdx.x / bhn);  // longest first
-    const int bh = (int)(blockIdx.x % bhn), b = bh / a.H, h = bh % a.H;
+    // work items longest first: later query tiles (causal ones see more keys) first, or, with
+    // per-sequence key lengths, longer sequences first
+    int qt, b, h;
+    if (a.kv_lens && a.B <= 32) {
+        const int per_b = a.H * a.n_items;
+        const int rem = (int)(blockIdx.x % per_b);
+        qt = a.n_items - 1 - rem / a.H;
+        h = rem % a.H;
+        b = batch_by_rank(a, (int)(blockIdx.x / per_b));
+    } else {
+        const int bhn = a.B * a.H;
+        qt = a.n_items - 1 - (int)(blockIdx.x / bhn);
+        const int bh = (int)(blockIdx.x % bhn);
+        b = bh / a.H;
+        h = bh % a.H;
+    }
     const int q0 = qt * BQ;
 
     const int n = seq_len(a, b, threadIdx.x == 0 && qt == 0 && h == 0);
