@@ -141,6 +141,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (the job is as slow as its slowest replica)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms, scale=1e12):
+    """Whole-job throughput: the units all `world` replicas processed over the slowest rank's
+    time per step (`scale` 1e12 for TFLOP/s, 1e9 for GB/s)."""
+    return world * units_per_rank / (ms / 1e3) / scale
+
+
 def cpu_oracle_sample(a, seconds_target, seed=0):
     """Time the float64 oracle on whole heads of workload `a` (taken in a fixed seeded order)
     until about `seconds_target` of CPU work; returns (TFLOP/s, sample description, threads)."""
@@ -263,13 +280,9 @@ def run_ours(args):
     ms = sum(ms_steps) / len(ms_steps)
     if ofa.device_error_flags() & 1:
         raise RuntimeError("a kernel gave up a bounded wait during the timed region")
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * flops / (ms / 1e3) / 1e12
-    achieved = flops / (ms / 1e3) / 1e12
+    ms = max_over_ranks(ms, world, dev)
+    value = job_rate(world, flops, ms)
+    achieved = job_rate(1, flops, ms)
 
     # end to end through the public API: pinned host inputs in, o and lse out, every step.  The
     # steps are pipelined the way a serving loop runs them: step k's inputs copy in on one
@@ -323,11 +336,7 @@ def run_ours(args):
     ee.record(s_out)
     barrier()
     ms_e2e = es.elapsed_time(ee) / n_e2e
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(ms_e2e, world, dev)
     del dqkv, dout, hq, hk, hv, ho, hl
 
     # split-KV decode on the long-cache workload (its own roofline: HBM)
@@ -353,9 +362,10 @@ def run_ours(args):
             dstep()
         de.record(stream)
         barrier()
-        ms_d = ds.elapsed_time(de) / nd
-        gbs = d.kv_bytes() / (ms_d / 1e3) / 1e9
-        dec = {"workload": "bf16_decode_b64_h32_l8192_d128_splits16", "value": gbs,
+        ms_d = max_over_ranks(ds.elapsed_time(de) / nd, world, dev)
+        gbs = job_rate(1, d.kv_bytes(), ms_d, 1e9)  # one GPU's rate, against one GPU's peak
+        dec = {"workload": "bf16_decode_b64_h32_l8192_d128_splits16",
+               "value": job_rate(world, d.kv_bytes(), ms_d, 1e9),
                "unit": "GB/s", "ms_per_step": ms_d, "steps": nd,
                "kv_bytes_per_step": d.kv_bytes(), "gpu_launches_per_step": 2,
                "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
@@ -374,7 +384,7 @@ def run_ours(args):
                    "causal": True, "flops_per_step": flops, "l2": "flushed before every step",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps,
-        "e2e": {"value": world * flops / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_rate(world, flops, ms_e2e), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "pipelining": "step k copies in while step k-1 computes and step k-2 copies out"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
