@@ -109,3 +109,32 @@ def test_bf16_cuda_graph_replay():
         assert ofa.device_error_flags() & 1 == 0
         o_ref, l_ref, _ = oracle_full(b)
         compare(o, lse, o_ref, l_ref, torch.bfloat16, what=f"graph replay seed {seed}")
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_bias_in_the_two_tile_kernel(dk, dv, causal):
+    # fp32 bias with explicit -inf masks and padded sequences, several items per CTA; with one
+    # visible key in the last sequence some rows are emptied by the bias alone, and the oracle's
+    # -inf lse marks them (compare checks those rows are exactly +0.0 / -inf)
+    a = wl.make_prefill(3, 6, 600, 650, dk, dv, torch.bfloat16, causal=causal, bias=True,
+                        kv_lens=[650, 333, 1], seed=39, device=DEV, bias_mask_p=0.05)
+    o, lse = run(a)
+    o_ref, l_ref, _ = oracle_full(a)
+    assert np.all(np.isinf(l_ref)[empty_rows(a)])  # every row the mask empties is among them
+    compare(o, lse, o_ref, l_ref, torch.bfloat16, what=f"bias {dk}/{dv} causal={causal}")
+
+
+@pytest.mark.parametrize("dk", [128, 192])
+def test_bf16_broadcast_bias_over_batch_and_heads(dk):
+    # one [Nq, Nk] bias for every (b, h): batch and head strides 0 (with dk = 192 the bias
+    # cannot go through a tensor map and is read with plain loads)
+    a = wl.make_prefill(2, 4, 400, 400, dk, 128, torch.bfloat16, causal=False, seed=40,
+                        device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(41)
+    base = torch.randn((1, 1, 400, 400), generator=g, device=DEV, dtype=torch.float32)
+    a.bias = base.expand(a.B, a.H, 400, 400)
+    o, lse = run(a)
+    o_ref, l_ref, _ = oracle_full(a)
+    compare(o, lse, o_ref, l_ref, torch.bfloat16, what=f"broadcast bias dk={dk}")
