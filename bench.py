@@ -423,6 +423,8 @@ CASES = {
     "fp32": ("fp32_small", {}, "fwd"),
     "decode": ("decode", {}, "decode"),
     "decode_b16": ("decode", {"B": 16}, "decode"),
+    "decode_nq4": ("decode", {"nq": 4, "causal": True}, "decode"),
+    "decode_nq8": ("decode", {"nq": 8, "causal": True}, "decode"),
 }
 
 
@@ -444,13 +446,13 @@ def run_case(args):
                                   scale=a.scale, out=o, lse=lse)
         work, unit = a.flops() / 1e12, "TFLOP/s"
     else:
-        ws = torch.empty(ofa.decode_workspace_bytes(a.B, a.H, a.dv, a.num_splits) // 4,
+        ws = torch.empty(ofa.decode_workspace_bytes(a.B, a.H, a.dv, a.num_splits, a.Nq) // 4,
                          dtype=torch.float32, device=dev)
-        o = torch.empty((a.B, 1, a.H, a.dv), dtype=a.q.dtype, device=dev)
-        lse = torch.empty((a.B, a.H, 1), dtype=torch.float32, device=dev)
+        o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
+        lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
         fn = lambda: ofa.attn_decode_splitkv(a.q, a.k, a.v, kv_lens=a.kv_lens, bias=a.bias,
                                              num_splits=a.num_splits, scale=a.scale,
-                                             workspace=ws, out=o, lse=lse)
+                                             workspace=ws, out=o, lse=lse, causal=a.causal)
         work, unit = a.kv_bytes() / 1e9, "GB/s"
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(args.warmup):

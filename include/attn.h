@@ -124,26 +124,36 @@ typedef struct {
 attn_status_t attn_fwd(const attn_fwd_params_t *params, attn_stream_t stream);
 
 /*
- * Size in bytes of the workspace attn_decode_splitkv needs: the per-split partial states,
- * float32 [B, H, num_splits, 2 + dv] laid out (m, l, u[0..dv)), where m is the maximum
- * logit of the split (natural-log units), l = sum exp(x_j - m) and u = sum exp(x_j - m) v_j
- * over the split's visible keys; an empty split is (-inf, 0, 0...).
+ * Size in bytes of the workspace attn_decode_splitkv needs for Nq query rows per sequence:
+ * the per-split partial states, float32 [B, H, Nq, num_splits, 2 + dv] laid out
+ * (m, l, u[0..dv)), where m is the maximum logit of the split (natural-log units),
+ * l = sum exp(x_j - m) and u = sum exp(x_j - m) v_j over the keys of the split visible to
+ * that row; an empty split is (-inf, 0, 0...).  Returns 0 for a negative or zero size.
  */
+size_t attn_decode_workspace_bytes_rows(int64_t B, int64_t H, int64_t Nq, int64_t dv,
+                                        int32_t num_splits);
+
+/* attn_decode_workspace_bytes_rows with Nq = 1: float32 [B, H, num_splits, 2 + dv]. */
 size_t attn_decode_workspace_bytes(int64_t B, int64_t H, int64_t dv, int32_t num_splits);
 
 /*
- * attn_decode_splitkv -- one query row per (b, h) (params->Nq must be 1) against a long
- * key/value cache, the keys of each sequence split into num_splits contiguous near-equal
- * ranges of [0, n_b) (split s covers [floor(s*n_b/S), floor((s+1)*n_b/S))).
+ * attn_decode_splitkv -- a few query rows per (b, h) (1 <= params->Nq <= 8: one decode
+ * step, or several tokens of one sequence at once) against a long key/value cache, the keys
+ * of each sequence split into num_splits contiguous near-equal ranges of [0, n_b) (split s
+ * covers [floor(s*n_b/S), floor((s+1)*n_b/S))).  Each key row of the cache is read once for
+ * all Nq query rows.  params->causal applies the bottom-right mask of the conventions above
+ * (row i sees keys j <= i + n_b - Nq), so the last row sees the whole sequence; a row that
+ * sees no key is empty.
  * ("How Does FlashAttention Preserve Global Softmax Across Tiles?", section 8, decode;
- *  section 3, merge.)
+ *  section 6, bottom-right alignment; section 3, merge.)
  * Queues two kernels on `stream`: the split kernel writes every partial state into
  * `workspace` (layout above), then the merge kernel writes o and lse exactly as attn_fwd
  * would.  The workspace is caller-owned device memory of at least
- * attn_decode_workspace_bytes(...) bytes, 16-byte aligned; after the call it holds the
- * partial states.  Supported: bfloat16, dk == dv in {64, 128}, 1 <= num_splits <= 256.
- * The cache may use any strides that keep each key row contiguous and 16-byte aligned
- * (e.g. a [B, H, L, d] cache passed with k_stride = {H*L*d, d, L*d}).
+ * attn_decode_workspace_bytes_rows(B, H, Nq, dv, num_splits) bytes, 16-byte aligned; after
+ * the call it holds the partial states.  Supported: bfloat16, dk == dv in {64, 128},
+ * 1 <= num_splits <= 256.  Nq outside [1, 8] returns ATTN_ERR_INVALID_ARG.  The cache may
+ * use any strides that keep each key row contiguous and 16-byte aligned (e.g. a [B, H, L, d]
+ * cache passed with k_stride = {H*L*d, d, L*d}).
  */
 attn_status_t attn_decode_splitkv(const attn_fwd_params_t *params, int32_t num_splits,
                                   void *workspace, size_t workspace_bytes,
@@ -156,7 +166,7 @@ attn_status_t attn_decode_splitkv(const attn_fwd_params_t *params, int32_t num_s
  * synchronise the device).  The paper has no counterpart: the pages describe no such variant.
  *   - Same arguments, checks, kernels and results as attn_decode_splitkv, without the
  *     workspace: the partial states go to a device array built into the library, 32 MiB
- *     (B * H * num_splits * (2 + dv) * 4 bytes must fit; larger problems return
+ *     (B * H * Nq * num_splits * (2 + dv) * 4 bytes must fit; larger problems return
  *     ATTN_ERR_WORKSPACE and queue nothing).  Every device that loads the library holds that
  *     array until the process exits.  No device memory is allocated by any call.
  *   - The first call on a device looks up the array's device address (with that device

@@ -89,6 +89,8 @@ def load():
         lib.attn_fwd.restype = i32
         lib.attn_decode_workspace_bytes.argtypes = [i64, i64, i64, i32]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_workspace_bytes_rows.argtypes = [i64, i64, i64, i64, i32]
+        lib.attn_decode_workspace_bytes_rows.restype = ctypes.c_size_t
         lib.attn_decode_splitkv.argtypes = [P, i32, vp, ctypes.c_size_t, vp]
         lib.attn_decode_splitkv.restype = i32
         lib.attn_decode_splitkv_noalloc.argtypes = [P, i32, vp]
@@ -202,17 +204,18 @@ def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, block_k
     return out, lse
 
 
-def decode_workspace_bytes(B, H, dv, num_splits) -> int:
-    return int(load().attn_decode_workspace_bytes(B, H, dv, num_splits))
+def decode_workspace_bytes(B, H, dv, num_splits, Nq=1) -> int:
+    return int(load().attn_decode_workspace_bytes_rows(B, H, Nq, dv, num_splits))
 
 
 def attn_decode_splitkv(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=None,
-                        workspace=None, out=None, lse=None, stream=None):
-    """Split-KV decode (q [B, 1, H, d]); returns (o, lse, workspace).
+                        workspace=None, out=None, lse=None, stream=None, causal=False):
+    """Split-KV decode (q [B, Nq, H, d], 1 <= Nq <= 8); returns (o, lse, workspace).
 
     k, v are [B, L, H, d]-indexed views (a [B, H, L, d] cache passes as
-    ``cache.permute(0, 2, 1, 3)``).  The workspace holds the partial states
-    [B, H, num_splits, 2 + dv] (m, l, u) after the call."""
+    ``cache.permute(0, 2, 1, 3)``).  causal applies the bottom-right mask (row i sees keys
+    j <= i + kv_len - Nq).  The workspace holds the partial states
+    [B, H, Nq, num_splits, 2 + dv] (m, l, u) after the call."""
     lib = load()
     B, Nq, H, _ = q.shape
     dv = v.shape[3]
@@ -220,18 +223,18 @@ def attn_decode_splitkv(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=N
         out = torch.empty((B, Nq, H, dv), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes(B, H, dv, num_splits)
+    need = decode_workspace_bytes(B, H, dv, num_splits, Nq)
     if workspace is None:
         workspace = torch.empty((max(need, 16) + 3) // 4, dtype=torch.float32, device=q.device)
     _require_cuda(workspace)
-    p = make_params(q, k, v, out, lse, bias, kv_lens, False, scale, 0)
+    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, 0)
     _check(lib.attn_decode_splitkv(ctypes.byref(p), int(num_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse, workspace
 
 
 def attn_decode_splitkv_noalloc(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=None,
-                                out=None, lse=None, stream=None):
+                                out=None, lse=None, stream=None, causal=False):
     """Split-KV decode that allocates no device memory in the library: for callers that
     cannot allocate while decoding.  The partial states go to a 32 MiB device array built
     into the library (shared by every call: order calls on one stream).  The first call on a
@@ -244,7 +247,7 @@ def attn_decode_splitkv_noalloc(q, k, v, kv_lens=None, num_splits=16, bias=None,
         out = torch.empty((B, Nq, H, dv), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    p = make_params(q, k, v, out, lse, bias, kv_lens, False, scale, 0)
+    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, 0)
     _check(lib.attn_decode_splitkv_noalloc(ctypes.byref(p), int(num_splits), _stream(stream)))
     return out, lse
 

@@ -140,9 +140,14 @@ extern "C" attn_status_t attn_fwd(const attn_fwd_params_t *p, attn_stream_t stre
     return launch_fwd_bf16(*p, s);
 }
 
+extern "C" size_t attn_decode_workspace_bytes_rows(int64_t B, int64_t H, int64_t Nq, int64_t dv,
+                                                   int32_t num_splits) {
+    if (B < 0 || H < 0 || Nq < 1 || dv < 1 || num_splits < 1) return 0;
+    return (size_t)B * (size_t)H * (size_t)Nq * (size_t)num_splits * (size_t)(2 + dv) * sizeof(float);
+}
+
 extern "C" size_t attn_decode_workspace_bytes(int64_t B, int64_t H, int64_t dv, int32_t num_splits) {
-    if (B < 0 || H < 0 || dv < 1 || num_splits < 1) return 0;
-    return (size_t)B * (size_t)H * (size_t)num_splits * (size_t)(2 + dv) * sizeof(float);
+    return attn_decode_workspace_bytes_rows(B, H, 1, dv, num_splits);
 }
 
 extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t num_splits,
@@ -151,7 +156,9 @@ extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t
     g_msg[0] = 0;
     attn_status_t st = check_common(p);
     if (st) return st;
-    if (p->Nq != 1) return fail(ATTN_ERR_INVALID_ARG, "decode needs Nq == 1 (got %lld)", (long long)p->Nq);
+    if (p->Nq < 1 || p->Nq > attn::kMaxDecodeRows)
+        return fail(ATTN_ERR_INVALID_ARG, "decode needs 1 <= Nq <= %d (got %lld)", attn::kMaxDecodeRows,
+                    (long long)p->Nq);
     if (num_splits < 1 || num_splits > 256)
         return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [1, 256] (got %d)", num_splits);
     if (p->dtype != ATTN_DTYPE_BF16)
@@ -165,14 +172,14 @@ extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t
     if (!stride_mult(p->q_stride, 8) || !stride_mult(p->k_stride, 8) ||
         !stride_mult(p->v_stride, 8) || !stride_mult(p->o_stride, 8))
         return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
-    size_t need = attn_decode_workspace_bytes(p->B, p->H, p->dv, num_splits);
+    size_t need = attn_decode_workspace_bytes_rows(p->B, p->H, p->Nq, p->dv, num_splits);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)",
                     need, workspace_bytes);
     float *part = static_cast<float *>(workspace);
     st = launch_decode_split(*p, num_splits, part, reinterpret_cast<cudaStream_t>(stream));
     if (st) return st;
-    return launch_merge(part, p->B, p->H, num_splits, p->dv, p->dtype, p->o, p->o_stride, p->lse,
+    return launch_merge(part, p->B, p->H, p->Nq, num_splits, p->dv, p->dtype, p->o, p->o_stride, p->lse,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -191,7 +198,7 @@ extern "C" attn_status_t attn_merge_states(const float *partials, int64_t B, int
     if (!partials || !o || !o_stride) return fail(ATTN_ERR_INVALID_ARG, "partials, o or o_stride is NULL");
     for (int i = 0; i < 3; ++i)
         if (o_stride[i] < 0) return fail(ATTN_ERR_INVALID_ARG, "o_stride[%d] is negative", i);
-    return launch_merge(partials, B, H, num_splits, dv, o_dtype, o, o_stride, lse,
+    return launch_merge(partials, B, H, 1, num_splits, dv, o_dtype, o, o_stride, lse,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 

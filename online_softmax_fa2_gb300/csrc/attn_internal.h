@@ -22,9 +22,12 @@ attn_status_t launch_fwd_f32(const attn_fwd_params_t &p, cudaStream_t s);
 attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s);
 attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
                                   cudaStream_t s);
-attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int num_splits,
+attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t Nq, int num_splits,
                            int64_t dv, int o_dtype, void *o, const int64_t o_stride[3],
                            float *lse, cudaStream_t s);
+
+// Largest number of query rows per sequence the split-KV decode takes.
+constexpr int kMaxDecodeRows = 8;
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

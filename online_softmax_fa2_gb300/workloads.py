@@ -15,6 +15,8 @@ Five standard workloads (names are what they are, with their sizes):
                                whose logit is raised by +8 (through q, see below)
   bf16_decode_b64_h32_l8192_d128  bf16 decode, B=64, H=32, Nq=1, cache 8192,
                                kv_len ~ U{1..8192} (kv_len[0]=1, kv_len[63]=8192), 16 splits
+                               (decode(..., nq=4, causal=True): four query rows per sequence,
+                               aligned to its end)
 
 Layouts: q, o [B, N, H, d] (b, n, h, d order); k, v [B, N, H, d] for prefill and a
 [B, H, L, d] cache for decode (passed to the library as strided views); bias [B, H, Nq, Nk]
@@ -180,15 +182,17 @@ def long_causal(device="cpu", seed=4, B=1, H=32, N=16384, d=128):
 
 
 def decode(device="cpu", seed=5, B=64, H=32, L=8192, d=128, num_splits=16, poison=True,
-           lens=None):
-    """Split-KV decode: one query row per (b, h) against a [B, H, L, d] cache."""
+           lens=None, nq=1, causal=False):
+    """Split-KV decode: nq query rows per (b, h) (1 for one decode step; a few for several
+    tokens of a sequence at once, with causal=True aligning them to the end of the
+    sequence) against a [B, H, L, d] cache."""
     if lens is None:
         gl = _gen("cpu", seed + 1000)
         lens = torch.randint(1, L + 1, (B,), generator=gl).tolist()
         if B >= 2:
             lens[0], lens[B - 1] = 1, L
     g = _gen(device, seed)
-    q = randn((B, 1, H, d), g, device, torch.bfloat16)
+    q = randn((B, nq, H, d), g, device, torch.bfloat16)
     kc = randn((B, H, L, d), g, device, torch.bfloat16)
     vc = randn((B, H, L, d), g, device, torch.bfloat16)
     kvl = torch.tensor(lens, dtype=torch.int32, device=device)
@@ -200,8 +204,9 @@ def decode(device="cpu", seed=5, B=64, H=32, L=8192, d=128, num_splits=16, poiso
     # the library takes [B, N, H, d]-ordered strided views; the cache is [B, H, L, d] in memory
     k = kc.permute(0, 2, 1, 3)
     v = vc.permute(0, 2, 1, 3)
-    return Attn(f"bf16_decode_b{B}_h{H}_l{L}_d{d}", torch.bfloat16, B, H, 1, L, d, d, False,
-                1.0 / math.sqrt(d), q, k, v, None, kvl, num_splits)
+    name = f"bf16_decode_b{B}_h{H}_l{L}_d{d}" + (f"_nq{nq}" if nq > 1 else "") + ("_causal" if causal else "")
+    return Attn(name, torch.bfloat16, B, H, nq, L, d, d, causal, 1.0 / math.sqrt(d), q, k, v, None,
+                kvl, num_splits)
 
 
 STANDARD = {

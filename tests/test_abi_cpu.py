@@ -40,6 +40,8 @@ def test_version_and_workspace_size(lib):
     assert lib.attn_version() >= 100
     assert ofa.decode_workspace_bytes(64, 32, 128, 16) == 64 * 32 * 16 * 130 * 4
     assert ofa.decode_workspace_bytes(-1, 32, 128, 16) == 0
+    assert ofa.decode_workspace_bytes(64, 32, 128, 16, Nq=4) == 4 * 64 * 32 * 16 * 130 * 4
+    assert ofa.decode_workspace_bytes(64, 32, 128, 16, Nq=0) == 0
 
 
 def _params(**kw):
@@ -91,8 +93,15 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert lib.attn_decode_splitkv(ctypes.byref(p), 300, ws, 1 << 20, None) == ofa.Status.INVALID_ARG
     assert lib.attn_decode_splitkv(ctypes.byref(p), 4, ws, 16, None) == ofa.Status.WORKSPACE
     assert lib.attn_decode_splitkv(ctypes.byref(p), 4, None, 1 << 20, None) == ofa.Status.WORKSPACE
-    p2 = _params(Nq=2)
+    p2 = _params(Nq=9)  # more query rows than the decode takes
     assert lib.attn_decode_splitkv(ctypes.byref(p2), 4, ws, 1 << 20, None) == ofa.Status.INVALID_ARG
+    p2 = _params(Nq=0)
+    assert lib.attn_decode_splitkv(ctypes.byref(p2), 4, ws, 1 << 20, None) == ofa.Status.INVALID_ARG
+    # Nq rows need Nq times the partial states of one row
+    p2 = _params(Nq=3)
+    one = lib.attn_decode_workspace_bytes(p2.B, p2.H, p2.dv, 4)
+    assert lib.attn_decode_workspace_bytes_rows(p2.B, p2.H, 3, p2.dv, 4) == 3 * one
+    assert lib.attn_decode_splitkv(ctypes.byref(p2), 4, ws, 3 * one - 16, None) == ofa.Status.WORKSPACE
     p3 = _params(Nq=1, dtype=0)
     assert lib.attn_decode_splitkv(ctypes.byref(p3), 4, ws, 1 << 20, None) == ofa.Status.UNSUPPORTED
     p4 = _params(Nq=1, dk=128, dv=64)
