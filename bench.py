@@ -425,6 +425,7 @@ CASES = {
     "decode_b16": ("decode", {"B": 16}, "decode"),
     "decode_nq4": ("decode", {"nq": 4, "causal": True}, "decode"),
     "decode_nq8": ("decode", {"nq": 8, "causal": True}, "decode"),
+    "decode_nq4_b16": ("decode", {"B": 16, "nq": 4, "causal": True}, "decode"),
 }
 
 

@@ -8,7 +8,11 @@
 // "Flash attention and efficient attention: Visual walkthrough", Step 5).  Empty parts are
 // skipped; a row whose parts are all empty gives o = +0.0, lse = -inf (section 6).
 //
-// Split kernel: grid (S, H, B), 128 threads.  The cache is read once, with 16-byte loads:
+// Several query rows of one sequence (2 <= Nq <= 8, bottom-right causal optional) share one
+// pass over the cache: see decode_rows_mma_kernel below.  Partial states are laid out
+// [B, H, Nq, S, 2 + D]; the merge kernel takes one (b, h, row) per CTA.
+//
+// Split kernel (one row): grid (S, H, B), 128 threads.  The cache is read once, with 16-byte loads:
 // a group of D/8 lanes holds one key row (each lane 8 bf16 of K and 8 of V), so a warp
 // reads 32/(D/8) key rows per load instruction, coalesced.  Each group runs the online
 // update over its keys (key lo + g + t*G of the split for t = 0, 1, ..., G groups per CTA,
@@ -64,19 +68,17 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return r;
 }
 
-// R: query rows handled per CTA (Nq <= R; rows Nq..R-1 are padding and do nothing).  Every
-// key row is read once for all R query rows.
-template <int D, int R>
+// One query row (Nq == 1; with one row the bottom-right causal mask hides no key).
+template <int D>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
     constexpr int LPK = D / 8;            // lanes per key row
     constexpr int G = kThreads / LPK;     // key groups per CTA
-    constexpr int U = R <= 2 ? 4 : 2;     // keys in flight per group
-    __shared__ float sm_m[R][G], sm_l[R][G];
-    __shared__ float sm_u[R][G][D + 1];
+    constexpr int U = 4;                  // keys in flight per group
+    __shared__ float sm_m[G], sm_l[G];
+    __shared__ float sm_u[G][D + 1];
 
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int g = threadIdx.x / LPK, sub = threadIdx.x % LPK, c0 = sub * 8;
-    const int nq = a.Nq;
 
     int n = a.Nk;
     if (a.kv_lens) {
@@ -86,36 +88,18 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
     }
     const int lo = (int)(((long long)s * n) / a.S), hi = (int)(((long long)(s + 1) * n) / a.S);
 
-    // row r sees keys j < vis[r]: j < n, and, when causal, j <= r + n - Nq (the sequences'
-    // ends aligned, "bottom-right"); a row with vis <= 0 sees no key
-    int vis[R];
-    float qf[R][8];
-    const float *bias_row[R];
+    float qf[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.q + b * a.qs0 + h * a.qs2 + c0), qf);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        vis[r] = r < nq ? (a.causal ? min(n, max(0, r + n - nq + 1)) : n) : 0;
-        bias_row[r] = (a.bias && r < nq) ? a.bias + b * a.bs0 + h * a.bs1 + r * a.bs2 : nullptr;
-        if (r < nq) {
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.q + b * a.qs0 + r * a.qs1 + h * a.qs2 + c0), qf[r]);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) qf[r][t] *= a.scale_log2;
-        } else {
-#pragma unroll
-            for (int t = 0; t < 8; ++t) qf[r][t] = 0.f;
-        }
-    }
+    for (int t = 0; t < 8; ++t) qf[t] *= a.scale_log2;
 
     const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks2 + c0;
     const __nv_bfloat16 *vb = a.v + b * a.vs0 + h * a.vs2 + c0;
+    const float *bias_row = a.bias ? a.bias + b * a.bs0 + h * a.bs1 : nullptr;
 
-    float m[R], l[R], u[R][8];
+    float m = -INFINITY, l = 0.f, u[8];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        m[r] = -INFINITY;
-        l[r] = 0.f;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) u[r][t] = 0.f;
-    }
+    for (int t = 0; t < 8; ++t) u[t] = 0.f;
 
     // Every thread runs the same iterations (the shuffles below need the whole warp);
     // key base + w*G + g belongs to group g.
@@ -131,70 +115,302 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
                 vr[w] = ld_stream(vb + (long long)j * a.vs1);
             }
         }
-        float x[R][U];
+        float x[U];
 #pragma unroll
         for (int w = 0; w < U; ++w) {
             float kf[8];
             bf16x8_to_f32(kr[w], kf);
+            float d = 0.f;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float d = 0.f;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) d = fmaf(qf[r][t], kf[t], d);
-                x[r][w] = d;
-            }
+            for (int t = 0; t < 8; ++t) d = fmaf(qf[t], kf[t], d);
+            x[w] = d;
         }
 #pragma unroll
         for (int w = 0; w < U; ++w) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-#pragma unroll
-                for (int o = LPK / 2; o > 0; o >>= 1) x[r][w] += __shfl_xor_sync(0xffffffffu, x[r][w], o);
-            }
+            for (int o = LPK / 2; o > 0; o >>= 1) x[w] += __shfl_xor_sync(0xffffffffu, x[w], o);
         }
 #pragma unroll
         for (int w = 0; w < U; ++w) {
             const int j = base + w * G + g;
             if (j >= hi) break;  // uniform across the group
+            float xs = x[w];
+            if (bias_row) {
+                float bj = bias_row[j];
+                if (bj == -INFINITY) continue;  // masked key
+                xs = fmaf(bj, kLog2e, xs);
+            }
+            float m_new = fmaxf(m, xs);
+            float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
+            float p = ex2(xs - m_new);
             float vf[8];
             bf16x8_to_f32(vr[w], vf);
+            l = fmaf(alpha, l, p);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (j >= vis[r]) continue;  // masked (or a padding row); uniform across the group
-                float xs = x[r][w];
-                if (bias_row[r]) {
-                    const float bj = bias_row[r][j];
-                    if (bj == -INFINITY) continue;  // masked key
-                    xs = fmaf(bj, kLog2e, xs);
-                }
-                const float m_new = fmaxf(m[r], xs);
-                const float alpha = (m[r] == -INFINITY) ? 0.f : ex2(m[r] - m_new);
-                const float p = ex2(xs - m_new);
-                l[r] = fmaf(alpha, l[r], p);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) u[r][t] = fmaf(alpha, u[r][t], p * vf[t]);
-                m[r] = m_new;
-            }
+            for (int t = 0; t < 8; ++t) u[t] = fmaf(alpha, u[t], p * vf[t]);
+            m = m_new;
         }
     }
 
+    if (sub == 0) {
+        sm_m[g] = m;
+        sm_l[g] = l;
+    }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        if (sub == 0) {
-            sm_m[r][g] = m[r];
-            sm_l[r][g] = l[r];
+    for (int t = 0; t < 8; ++t) sm_u[g][c0 + t] = u[t];
+    __syncthreads();
+
+    // merge the G group states; thread c owns column c
+    float M = -INFINITY;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg)
+        if (sm_l[gg] > 0.f) M = fmaxf(M, sm_m[gg]);
+    float *out = a.part + (((long long)b * a.H + h) * a.S + s) * (2 + D);
+    if (M == -INFINITY) {  // empty split
+        for (int c = threadIdx.x; c < D; c += kThreads) out[2 + c] = 0.f;
+        if (threadIdx.x == 0) {
+            out[0] = -INFINITY;
+            out[1] = 0.f;
         }
+        return;
+    }
+    float L = 0.f;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) sm_u[r][g][c0 + t] = u[r][t];
+    for (int gg = 0; gg < G; ++gg)
+        if (sm_l[gg] > 0.f) L = fmaf(ex2(sm_m[gg] - M), sm_l[gg], L);
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+        float acc = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg)
+            if (sm_l[gg] > 0.f) acc = fmaf(ex2(sm_m[gg] - M), sm_u[gg][c], acc);
+        out[2 + c] = acc;
+    }
+    if (threadIdx.x == 0) {
+        out[0] = M * kLn2;  // back to natural-log units: exp(x - m) == 2^(x*log2e - M)
+        out[1] = L;
+    }
+}
+
+// ---------------------------------------------------------------- several query rows (Nq >= 2)
+//
+// With 2 to 8 query rows per sequence the per-key work grows with the rows while the bytes
+// read stay those of one row, so the scores and the value sums go to the tensor cores
+// (mma.sync m16n8k16, bf16 inputs, fp32 accumulation; the products are 16 keys by at most 8
+// rows, far below what tcgen05 tiles are for).  Each warp takes 16-key tiles of the split in
+// turn (tile w, w + 4, ...), copied into shared memory with cp.async (double-buffered, rows
+// padded to 16 B past 2*D so that ldmatrix reads are free of bank conflicts; keys past the
+// split are zero-filled, so nothing stored past kv_len reaches a product):
+//   S = Q K^T     M = 16 query rows (rows >= Nq are zero), N = 8 keys, K = 16 dims per step;
+//                 the K operand comes from ldmatrix on the [key][dim] tile;
+//   O^T += V^T P^T  M = 16 dims, N = 8 query rows, K = 16 keys; V^T comes from ldmatrix.trans,
+//                 and P^T is the S accumulator itself: the fragment a thread holds of S (row
+//                 g, keys 2t, 2t+1 of each 8-key half) is the fragment it must supply of P^T.
+// The online update runs per query row on the four lanes that hold it (row max over their
+// eight scores and two shuffles); the row's rescale factor reaches the lanes holding that row
+// of O^T by a shuffle.  At the end the four warps' states are merged in shared memory and the
+// split's state of each row is written as in the one-row kernel.
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// four 8x8 b16 matrices; lane i gives the address of row i % 8 of matrix i / 8
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// d += a * b for one m16n8k16 tile: a row-major 16x16 bf16, b 16x8 bf16 (k-major columns)
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+constexpr int kRowsKT = 16;  // keys per warp tile
+constexpr int kRowsWarps = kThreads / 32;
+
+template <int D>
+struct RowsLayout {
+    static constexpr int kRowBytes = 2 * D + 16;               // padded key row
+    static constexpr int kTileBytes = kRowsKT * kRowBytes;     // one K or V tile
+    static constexpr int kBytes = kRowsWarps * 2 * 2 * kTileBytes;  // [warp][stage][K, V]
+    static_assert(kRowsWarps * 8 * (2 + D) * 4 <= kBytes, "merge area");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
+    using L = RowsLayout<D>;
+    constexpr int NK = D / 16;  // k-steps of S = Q K^T; 16-dim tiles of O^T
+    extern __shared__ __align__(128) uint8_t dsm[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int nq = a.Nq;
+
+    int n = a.Nk;
+    if (a.kv_lens) {
+        int raw = a.kv_lens[b];
+        n = min(max(raw, 0), a.Nk);
+        if (raw != n && threadIdx.x == 0 && s == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
+    }
+    const int lo = (int)(((long long)s * n) / a.S), hi = (int)(((long long)(s + 1) * n) / a.S);
+
+    // this lane's softmax row is g (keys < vis_g visible); its rows of O^T are 2t and 2t + 1
+    const int vis_g = g < nq ? (a.causal ? min(n, max(0, g + n - nq + 1)) : n) : 0;
+    const float *bias_g = (a.bias && g < nq) ? a.bias + b * a.bs0 + h * a.bs1 + g * a.bs2 : nullptr;
+    uint32_t qa[NK][2];  // A fragments of Q: row g, dims 16 kk + 2t (+1) and + 8 (+9)
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+        qa[kk][0] = qa[kk][1] = 0u;
+        if (g < nq) {
+            const __nv_bfloat16 *qr = a.q + b * a.qs0 + g * a.qs1 + h * a.qs2 + 16 * kk + 2 * t;
+            qa[kk][0] = *reinterpret_cast<const uint32_t *>(qr);
+            qa[kk][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+        }
+    }
+    float m_g = -INFINITY, l_g = 0.f;  // row g's reference and this lane's share of its sum
+    float o[NK][4];
+#pragma unroll
+    for (int mt = 0; mt < NK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + h * a.ks2;
+    const __nv_bfloat16 *vb = a.v + b * a.vs0 + h * a.vs2;
+    uint8_t *wsm = dsm + warp * 4 * L::kTileBytes;
+    const int ntiles = (hi - lo + kRowsKT - 1) / kRowsKT;
+    // tile T of the split into stage st: 16 keys x D dims of K and of V, 16 B per copy
+    auto issue = [&](int T, int st) {
+        uint8_t *sK = wsm + (2 * st) * L::kTileBytes, *sV = sK + L::kTileBytes;
+        const int j0 = lo + T * kRowsKT;
+#pragma unroll
+        for (int i = 0; i < kRowsKT * (D / 8) / 32; ++i) {
+            const int c = lane + 32 * i, key = c / (D / 8), ch = c % (D / 8);
+            const int j = j0 + key;
+            const bool in = j < hi;
+            const long long jj = in ? j : lo;  // a valid address even when nothing is copied
+            cp_async16(smem_addr(sK + key * L::kRowBytes + ch * 16), kb + jj * a.ks1 + ch * 8, in ? 16u : 0u);
+            cp_async16(smem_addr(sV + key * L::kRowBytes + ch * 16), vb + jj * a.vs1 + ch * 8, in ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+    int st = 0;
+    if (warp < ntiles) issue(warp, 0);
+    else cp_async_commit();
+    for (int T = warp; T < ntiles; T += kRowsWarps, st ^= 1) {
+        if (T + kRowsWarps < ntiles) issue(T + kRowsWarps, st ^ 1);
+        else cp_async_commit();
+        cp_async_wait<1>();
+        __syncwarp();
+        const uint8_t *sK = wsm + (2 * st) * L::kTileBytes, *sV = sK + L::kTileBytes;
+        // matrices (keys 0-7 | 8-15) x (dims +0-7 | +8-15); this lane's row address
+        const uint32_t rowoff = ((mi >> 1) * 8 + mr) * L::kRowBytes + (mi & 1) * 16;
+
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            uint32_t kf[4];
+            ldsm_x4(smem_addr(sK) + rowoff + kk * 32, kf);
+            mma_16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, kf[0], kf[1]);
+            mma_16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, kf[2], kf[3]);
+        }
+        // row g's scores: keys j0 + 2t, + 1 (first half), j0 + 8 + 2t, + 1 (second half)
+        const int j0 = lo + T * kRowsKT;
+        float x[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
+        float tm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int j = j0 + (e >> 1) * 8 + 2 * t + (e & 1);
+            float xs = x[e] * a.scale_log2;
+            if (j >= hi || j >= vis_g) xs = -INFINITY;
+            else if (bias_g) {
+                const float bj = bias_g[j];
+                xs = (bj == -INFINITY) ? -INFINITY : fmaf(bj, kLog2e, xs);
+            }
+            x[e] = xs;
+            tm = fmaxf(tm, xs);
+        }
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+        const float m_new = fmaxf(m_g, tm);
+        const float alpha = (m_g == -INFINITY) ? 0.f : ex2(m_g - m_new);
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = (m_new == -INFINITY) ? 0.f : ex2(x[e] - m_new);
+        l_g = fmaf(alpha, l_g, (p[0] + p[1]) + (p[2] + p[3]));
+        m_g = m_new;
+        // rows 2t and 2t + 1 of O^T take the factors of those rows (held by lanes 8t, 8t + 4)
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+        const uint32_t pb0 = pack_bf16(p[0], p[1]), pb1 = pack_bf16(p[2], p[3]);
+#pragma unroll
+        for (int mt = 0; mt < NK; ++mt) {
+            o[mt][0] *= a0;
+            o[mt][1] *= a1;
+            o[mt][2] *= a0;
+            o[mt][3] *= a1;
+            uint32_t vf[4];
+            ldsm_x4_trans(smem_addr(sV) + rowoff + mt * 32, vf);
+            mma_16816(o[mt], vf[0], vf[1], vf[2], vf[3], pb0, pb1);
+        }
+        __syncwarp();  // every lane is done with this stage before it is refilled
+    }
+    cp_async_wait<0>();
+    l_g += __shfl_xor_sync(0xffffffffu, l_g, 1);
+    l_g += __shfl_xor_sync(0xffffffffu, l_g, 2);
+    __syncthreads();  // the tiles are no longer read: their space holds the warps' states
+
+    float *sm_m = reinterpret_cast<float *>(dsm);        // [warp][8 rows]
+    float *sm_l = sm_m + kRowsWarps * 8;                 // [warp][8 rows]
+    float *sm_o = sm_l + kRowsWarps * 8;                 // [warp][8 rows][D]
+    if (t == 0) {
+        sm_m[warp * 8 + g] = m_g;
+        sm_l[warp * 8 + g] = l_g;
+    }
+#pragma unroll
+    for (int mt = 0; mt < NK; ++mt) {
+        float *r0 = sm_o + (warp * 8 + 2 * t) * D + 16 * mt + g;
+        float *r1 = r0 + D;
+        r0[0] = o[mt][0];
+        r1[0] = o[mt][1];
+        r0[8] = o[mt][2];
+        r1[8] = o[mt][3];
     }
     __syncthreads();
 
-    // merge the G group states of each row; thread c owns column c
+    // thread c owns column c of every row
     for (int r = 0; r < nq; ++r) {
         float M = -INFINITY;
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg)
-            if (sm_l[r][gg] > 0.f) M = fmaxf(M, sm_m[r][gg]);
+        for (int w = 0; w < kRowsWarps; ++w)
+            if (sm_l[w * 8 + r] > 0.f) M = fmaxf(M, sm_m[w * 8 + r]);
         float *out = a.part + ((((long long)b * a.H + h) * nq + r) * a.S + s) * (2 + D);
         if (M == -INFINITY) {  // empty split
             for (int c = threadIdx.x; c < D; c += kThreads) out[2 + c] = 0.f;
@@ -204,20 +420,20 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
             }
             continue;
         }
-        float L = 0.f;
+        float Lsum = 0.f;
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg)
-            if (sm_l[r][gg] > 0.f) L = fmaf(ex2(sm_m[r][gg] - M), sm_l[r][gg], L);
+        for (int w = 0; w < kRowsWarps; ++w)
+            if (sm_l[w * 8 + r] > 0.f) Lsum = fmaf(ex2(sm_m[w * 8 + r] - M), sm_l[w * 8 + r], Lsum);
         for (int c = threadIdx.x; c < D; c += kThreads) {
             float acc = 0.f;
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg)
-                if (sm_l[r][gg] > 0.f) acc = fmaf(ex2(sm_m[r][gg] - M), sm_u[r][gg][c], acc);
+            for (int w = 0; w < kRowsWarps; ++w)
+                if (sm_l[w * 8 + r] > 0.f) acc = fmaf(ex2(sm_m[w * 8 + r] - M), sm_o[(w * 8 + r) * D + c], acc);
             out[2 + c] = acc;
         }
         if (threadIdx.x == 0) {
-            out[0] = M * kLn2;  // back to natural-log units: exp(x - m) == 2^(x*log2e - M)
-            out[1] = L;
+            out[0] = M * kLn2;
+            out[1] = Lsum;
         }
     }
 }
@@ -259,6 +475,15 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const float *part, int 
     if (lse && threadIdx.x == 0) lse[row] = M + logf(L);
 }
 
+template <int D>
+cudaError_t launch_rows(const DecArgs &a, dim3 grid, cudaStream_t st) {
+    const int smem = RowsLayout<D>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(decode_rows_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_rows_mma_kernel<D><<<grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
@@ -282,18 +507,17 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
         return fail(ATTN_ERR_UNSUPPORTED, "decode supports 1 <= Nq <= %d (got %lld)", kMaxDecodeRows,
                     (long long)p.Nq);
     dim3 grid((unsigned)num_splits, (unsigned)p.H, (unsigned)p.B);
-#define ATTN_DECODE_LAUNCH(D_)                                                                 \
-    if (p.Nq == 1) decode_split_kernel<D_, 1><<<grid, kThreads, 0, st>>>(a);                 \
-    else if (p.Nq == 2) decode_split_kernel<D_, 2><<<grid, kThreads, 0, st>>>(a);            \
-    else if (p.Nq <= 4) decode_split_kernel<D_, 4><<<grid, kThreads, 0, st>>>(a);            \
-    else decode_split_kernel<D_, 8><<<grid, kThreads, 0, st>>>(a);
-    if (p.dk == 64) {
-        ATTN_DECODE_LAUNCH(64)
+    cudaError_t e = cudaSuccess;
+    if (p.Nq == 1) {
+        if (p.dk == 64) decode_split_kernel<64><<<grid, kThreads, 0, st>>>(a);
+        else decode_split_kernel<128><<<grid, kThreads, 0, st>>>(a);
+    } else if (p.dk == 64) {
+        e = launch_rows<64>(a, grid, st);
     } else {
-        ATTN_DECODE_LAUNCH(128)
+        e = launch_rows<128>(a, grid, st);
     }
-#undef ATTN_DECODE_LAUNCH
-    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode rows launch: %s", cudaGetErrorString(e));
+    e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode split launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }

@@ -98,15 +98,20 @@ def test_decode_rows_split_invariance_and_poison():
 
 
 def test_decode_rows_one_row_is_the_single_row_decode():
-    # the first row of a non-causal Nq=4 decode is the Nq=1 decode of that row
+    # the first row of a non-causal Nq=4 decode is the Nq=1 decode of that row (the two take
+    # different kernels, P in bf16 on the tensor cores against fp32 on the FMA pipe: equal
+    # within the bf16 tolerance, and the empty sequence exactly)
     a4 = wl.decode(DEV, seed=44, B=4, H=3, L=500, d=128, num_splits=16, lens=[500, 9, 0, 250], nq=4)
     o4, l4, _ = run(a4)
     q1 = a4.q[:, :1].contiguous()
     o1, l1, _ = ofa.attn_decode_splitkv(q1, a4.k, a4.v, kv_lens=a4.kv_lens, num_splits=16,
                                         scale=a4.scale)
     torch.cuda.synchronize()
-    assert torch.equal(o1[:, 0].view(torch.int16), o4[:, 0].view(torch.int16))
-    assert torch.equal(l1[:, :, 0], l4[:, :, 0])
+    fin = torch.isfinite(l1[:, :, 0])
+    assert torch.equal(fin, torch.isfinite(l4[:, :, 0])) and not fin[2].any()
+    assert torch.all(o4[2].view(torch.int16) == 0)
+    assert (o1[:, 0].float() - o4[:, 0].float()).abs().max().item() <= TOL[torch.bfloat16]["o"]
+    assert (l1[:, :, 0][fin] - l4[:, :, 0][fin]).abs().max().item() <= TOL[torch.bfloat16]["lse"]
 
 
 def test_decode_rows_rejects_too_many_rows():
