@@ -57,6 +57,8 @@ def bind(path: str):
     lib.oracle_key_state.restype = i32
     lib.oracle_merge_states.argtypes = [i64, i64, i64, vp, vp, vp]
     lib.oracle_merge_states.restype = i32
+    lib.oracle_attn_bwd.argtypes = [i64] * 6 + [vp] * 5 + [i32, f64, vp, vp, vp, vp, i32]
+    lib.oracle_attn_bwd.restype = i32
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     return lib
@@ -133,6 +135,31 @@ def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, rows=No
     if used < 0:
         raise ValueError("oracle_attn_fwd rejected its arguments")
     return o, lse, used
+
+
+def attn_bwd(q, k, v, dout, bias=None, kv_lens=None, causal=False, scale=None, threads=0,
+             lib=None):
+    """Gradients of sum(dout * O) in float64: returns (dQ [B, Nq, H, dk], dK [B, Nk, H, dk],
+    dV [B, Nk, H, dv], threads used).  dout [B, Nq, H, dv]; other arguments as attn_fwd.  The
+    bias is fixed (no gradient); empty rows pass no gradient."""
+    q, k, v, bias, dout = _f32(q), _f32(k), _f32(v), _f32(bias), _f32(dout)
+    kvl = _kvl(kv_lens)
+    B, H, Nq, Nk, dk, dv = _shapes(q, k, v)
+    if dout.shape != (B, Nq, H, dv):
+        raise ValueError(f"dout shape {dout.shape}")
+    if bias is not None and bias.shape != (B, H, Nq, Nk):
+        raise ValueError(f"bias shape {bias.shape}")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    dq = np.empty((B, Nq, H, dk), np.float64)
+    dkk = np.empty((B, Nk, H, dk), np.float64)
+    dvv = np.empty((B, Nk, H, dv), np.float64)
+    used = (lib or _load()).oracle_attn_bwd(B, H, Nq, Nk, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
+                                   _ptr(kvl), int(bool(causal)), float(scale), _ptr(dout), _ptr(dq),
+                                   _ptr(dkk), _ptr(dvv), int(threads))
+    if used < 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dkk, dvv, used
 
 
 def attn_probs(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, lib=None):

@@ -292,6 +292,105 @@ ORACLE_EXPORT int oracle_merge_states(int64_t n_rows, int64_t n_states, int64_t 
     return 0;
 }
 
+/*
+ * Gradients of the loss through O, by definition ("How Does FlashAttention Preserve Global
+ * Softmax Across Tiles?", section 7: with g_i the upstream gradient of row i, the softmax
+ * Jacobian's row reduction is c_i = sum_j p_ij (g_i . v_j), which equals g_i . o_i; the
+ * gradient with respect to the scaled logits is p_ij (g_i . v_j - c_i); the Q and K gradients
+ * carry the original scale).  Written out row by row with the probability row materialised:
+ *
+ *   p_ij  = exp(x_ij - m_i) / l_i on visible (i, j), 0 elsewhere (as in the forward)
+ *   dV_j  = sum_i p_ij g_i
+ *   dP_ij = g_i . v_j,   c_i = sum_j p_ij dP_ij,   dS_ij = p_ij (dP_ij - c_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j,   dK_j = scale * sum_i dS_ij q_i
+ *
+ * Readings: the bias is fixed input (no gradient is formed for it); an empty row has a
+ * constant zero output, so it passes no gradient (its p row is all zero).
+ * dout [B, Nq, H, dv]; dq [B, Nq, H, dk], dk [B, Nk, H, dk], dv [B, Nk, H, dv], float64.
+ * Returns the number of threads used, or -1 on bad arguments.
+ */
+ORACLE_EXPORT int oracle_attn_bwd(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t dk,
+                                  int64_t dv, const float *q, const float *k, const float *v,
+                                  const float *bias, const int32_t *kv_lens, int causal,
+                                  double scale, const float *dout, double *dq, double *dkey,
+                                  double *dval, int n_threads) {
+    problem_t p = {B, H, Nq, Nk, dk, dv, q, k, v, bias, kv_lens, causal, scale};
+    if (check_problem(&p) || (Nq > 0 && !dout)) return -1;
+    memset(dq, 0, sizeof(double) * (size_t)(B * Nq * H * dk));
+    memset(dkey, 0, sizeof(double) * (size_t)(B * Nk * H * dk));
+    memset(dval, 0, sizeof(double) * (size_t)(B * Nk * H * dv));
+    int used = 1;
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+#else
+    {
+#endif
+        double *prow = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double *dprow = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        /* one (b, h) per iteration: its dK and dV rows are written by this thread only */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            const int64_t b = bh / H, h = bh % H;
+            for (int64_t i = 0; i < Nq; ++i) {
+                /* the probability row */
+                double m = -INFINITY;
+                int64_t nvis = 0;
+                for (int64_t j = 0; j < Nk; ++j) {
+                    prow[j] = 0.0;
+                    if (!visible(&p, b, h, i, j)) continue;
+                    double x = logit(&p, b, h, i, j);
+                    prow[j] = x;
+                    if (nvis == 0 || x > m) m = x;
+                    ++nvis;
+                }
+                if (nvis == 0) continue; /* empty row: no gradient */
+                double l = 0.0;
+                for (int64_t j = 0; j < Nk; ++j) {
+                    if (!visible(&p, b, h, i, j)) continue;
+                    prow[j] = exp(prow[j] - m);
+                    l += prow[j];
+                }
+                for (int64_t j = 0; j < Nk; ++j) prow[j] /= l;
+                /* dP_ij = g_i . v_j and the row reduction c_i */
+                const float *gi = dout + ((b * Nq + i) * H + h) * dv;
+                double c = 0.0;
+                for (int64_t j = 0; j < Nk; ++j) {
+                    dprow[j] = 0.0;
+                    if (!visible(&p, b, h, i, j)) continue;
+                    const float *vj = value_row(&p, b, h, j);
+                    double d = 0.0;
+                    for (int64_t t = 0; t < dv; ++t) d += (double)gi[t] * (double)vj[t];
+                    dprow[j] = d;
+                    c += prow[j] * d;
+                }
+                const float *qi = q + ((b * Nq + i) * H + h) * dk;
+                double *dqi = dq + ((b * Nq + i) * H + h) * dk;
+                for (int64_t j = 0; j < Nk; ++j) {
+                    if (!visible(&p, b, h, i, j)) continue;
+                    const double ds = prow[j] * (dprow[j] - c);
+                    const float *kj = k + ((b * Nk + j) * H + h) * dk;
+                    double *dkj = dkey + ((b * Nk + j) * H + h) * dk;
+                    double *dvj = dval + ((b * Nk + j) * H + h) * dv;
+                    for (int64_t t = 0; t < dv; ++t) dvj[t] += prow[j] * (double)gi[t];
+                    for (int64_t t = 0; t < dk; ++t) {
+                        dqi[t] += scale * ds * (double)kj[t];
+                        dkj[t] += scale * ds * (double)qi[t];
+                    }
+                }
+            }
+        }
+        free(prow);
+        free(dprow);
+    }
+    return used;
+}
+
 ORACLE_EXPORT int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
