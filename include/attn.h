@@ -195,6 +195,51 @@ attn_status_t attn_merge_states(const float *partials, int64_t B, int64_t H, int
                                 int64_t dv, int32_t o_dtype, void *o, const int64_t o_stride[3],
                                 float *lse, attn_stream_t stream);
 
+/*
+ * Arguments of one attention backward: the forward's arguments and outputs (fwd.o and
+ * fwd.lse as the forward wrote them; fwd.lse is required), the upstream gradient of O, and
+ * the three gradients to write.
+ *   dout [B, Nq, H, dv]   bf16, with dout_stride (b, n, h; elements)
+ *   dq   [B, Nq, H, dk]   bf16, written;  dk [B, Nk, H, dk], dv [B, Nk, H, dv] likewise
+ */
+typedef struct {
+    attn_fwd_params_t fwd;
+    const void *dout;
+    int64_t dout_stride[3];
+    void *dq;
+    int64_t dq_stride[3];
+    void *dk;
+    int64_t dk_stride[3];
+    void *dv;
+    int64_t dv_stride[3];
+} attn_bwd_params_t;
+
+/*
+ * Size in bytes of the workspace attn_bwd needs: an fp32 dQ accumulator [B, Nq, H, dk] and
+ * the fp32 row terms c_i [B, H, Nq].  Returns 0 for a negative or zero size.
+ */
+size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk);
+
+/*
+ * attn_bwd -- gradients dQ, dK, dV of a loss through O = attention(Q, K, V) given the
+ * upstream gradient G = dL/dO.
+ * ("How Does FlashAttention Preserve Global Softmax Across Tiles?", section 7: the forward
+ *  saves each row's log-sum-exp L_i and its output; the backward rebuilds the probabilities
+ *  p_ij = exp(x_ij - L_i) tile by tile from Q, K, the fixed mask and bias, takes
+ *  c_i = g_i . o_i, dS_ij = p_ij (g_i . v_j - c_i), and accumulates dV_j += p_ij g_i,
+ *  dK_j += scale dS_ij q_i, dQ_i += scale dS_ij k_j.)
+ * The mask, bias, kv_lens and causal settings must be the forward's.  The bias is fixed: no
+ * gradient is formed for it.  An empty row (lse = -inf) passes no gradient, and a key that no
+ * row sees gets dK = dV = 0.
+ * Queues three kernels on `stream`.  Supported: bfloat16, dk == dv in {64, 128}; every tensor
+ * 16-byte aligned with strides that are multiples of 8 elements.  The workspace is
+ * caller-owned device memory of at least attn_bwd_workspace_bytes(B, H, Nq, dk) bytes,
+ * 16-byte aligned; its contents on entry do not matter.  dQ is accumulated with atomic
+ * additions, so its rounding can differ from run to run in the last bits.
+ */
+attn_status_t attn_bwd(const attn_bwd_params_t *params, void *workspace, size_t workspace_bytes,
+                       attn_stream_t stream);
+
 /* Message describing the last non-OK status returned on the calling thread ("" if none). */
 const char *attn_last_error(void);
 

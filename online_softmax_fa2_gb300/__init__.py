@@ -23,8 +23,8 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc", "attn_merge_states",
-           "decode_workspace_bytes",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
+           "attn_merge_states", "decode_workspace_bytes", "bwd_workspace_bytes",
            "device_error_flags", "last_error", "library_path", "load", "AttnError", "Status"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +69,17 @@ class Params(ctypes.Structure):
     ]
 
 
+class BwdParams(ctypes.Structure):
+    """Mirror of attn_bwd_params_t (include/attn.h)."""
+    _fields_ = [
+        ("fwd", Params),
+        ("dout", ctypes.c_void_p), ("dout_stride", ctypes.c_int64 * 3),
+        ("dq", ctypes.c_void_p), ("dq_stride", ctypes.c_int64 * 3),
+        ("dk", ctypes.c_void_p), ("dk_stride", ctypes.c_int64 * 3),
+        ("dv", ctypes.c_void_p), ("dv_stride", ctypes.c_int64 * 3),
+    ]
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -98,6 +109,10 @@ def load():
         lib.attn_merge_states.argtypes = [vp, i64, i64, i32, i64, i32, vp,
                                           ctypes.POINTER(ctypes.c_int64), vp, vp]
         lib.attn_merge_states.restype = i32
+        lib.attn_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd.argtypes = [ctypes.POINTER(BwdParams), vp, ctypes.c_size_t, vp]
+        lib.attn_bwd.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_device_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
@@ -250,6 +265,38 @@ def attn_decode_splitkv_noalloc(q, k, v, kv_lens=None, num_splits=16, bias=None,
     p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, 0)
     _check(lib.attn_decode_splitkv_noalloc(ctypes.byref(p), int(num_splits), _stream(stream)))
     return out, lse
+
+
+def bwd_workspace_bytes(B, H, Nq, dk) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, H, Nq, dk))
+
+
+def attn_bwd(q, k, v, o, lse, dout, bias=None, kv_lens=None, causal=False, scale=None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of a loss through o = attn_fwd(q, k, v, ...), given dout = dL/do
+    and the forward's o and lse (bfloat16, dk == dv in {64, 128}).  The mask, bias, kv_lens
+    and causal settings must be the forward's; the bias gets no gradient."""
+    lib = load()
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    if dout.shape != o.shape or dout.dtype != q.dtype:
+        raise ValueError("dout must have o's shape and dtype")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, Nq, d)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16) + 3) // 4, dtype=torch.float32, device=q.device)
+    _require_cuda(dout, dq, dk, dv, workspace)
+    p = BwdParams()
+    p.fwd = make_params(q, k, v, o, lse, bias, kv_lens, causal, scale, 0)
+    p.dout, p.dout_stride = dout.data_ptr(), _bnhd_strides(dout, "dout")
+    p.dq, p.dq_stride = dq.data_ptr(), _bnhd_strides(dq, "dq")
+    p.dk, p.dk_stride = dk.data_ptr(), _bnhd_strides(dk, "dk")
+    p.dv, p.dv_stride = dv.data_ptr(), _bnhd_strides(dv, "dv")
+    _check(lib.attn_bwd(ctypes.byref(p), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                        _stream(stream)))
+    return dq, dk, dv
 
 
 def attn_merge_states(partials, out_dtype=torch.bfloat16, out=None, lse=None, stream=None):

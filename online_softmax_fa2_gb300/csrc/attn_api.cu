@@ -202,6 +202,49 @@ extern "C" attn_status_t attn_merge_states(const float *partials, int64_t B, int
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk) {
+    if (B < 0 || H < 0 || Nq < 0 || dk < 1) return 0;
+    const size_t acc = (size_t)B * (size_t)H * (size_t)Nq * (size_t)dk * sizeof(float);
+    const size_t rows = (size_t)B * (size_t)H * (size_t)Nq * sizeof(float);
+    return ((acc + 15) & ~(size_t)15) + rows;
+}
+
+extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, size_t workspace_bytes,
+                                  attn_stream_t stream) {
+    g_msg[0] = 0;
+    if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+    const attn_fwd_params_t *f = &p->fwd;
+    attn_status_t st = check_common(f);
+    if (st) return st;
+    if (f->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward supports bfloat16 only");
+    if (f->dk != f->dv || (f->dk != 64 && f->dk != 128))
+        return fail(ATTN_ERR_UNSUPPORTED, "backward supports dk == dv in {64, 128} (dk=%lld dv=%lld)",
+                    (long long)f->dk, (long long)f->dv);
+    if ((st = check_strides("dout", p->dout_stride)) || (st = check_strides("dq", p->dq_stride)) ||
+        (st = check_strides("dk", p->dk_stride)) || (st = check_strides("dv", p->dv_stride)))
+        return st;
+    if (f->B * f->H * (f->Nq + f->Nk) == 0) return ATTN_OK;
+    if (f->Nq > 0 && (!f->lse || !p->dout || !p->dq))
+        return fail(ATTN_ERR_INVALID_ARG, "lse, dout and dq are required (lse as the forward wrote it)");
+    if (f->Nk > 0 && (!p->dk || !p->dv)) return fail(ATTN_ERR_INVALID_ARG, "dk or dv is NULL");
+    if (f->Nk > 0 && f->Nq > 0 && (!f->k || !f->v)) return fail(ATTN_ERR_INVALID_ARG, "k or v is NULL");
+    const void *ptrs[] = {f->q, f->k, f->v, f->o, p->dout, p->dq, p->dk, p->dv, f->lse};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return fail(ATTN_ERR_MISALIGNED, "every tensor must be 16-byte aligned");
+    if (!stride_mult(f->q_stride, 8) || !stride_mult(f->k_stride, 8) || !stride_mult(f->v_stride, 8) ||
+        !stride_mult(f->o_stride, 8) || !stride_mult(p->dout_stride, 8) || !stride_mult(p->dq_stride, 8) ||
+        !stride_mult(p->dk_stride, 8) || !stride_mult(p->dv_stride, 8))
+        return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
+    const size_t need = attn_bwd_workspace_bytes(f->B, f->H, f->Nq, f->dk);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)", need,
+                    workspace_bytes);
+    const size_t acc = (size_t)f->B * f->H * f->Nq * f->dk * sizeof(float);
+    float *dq_acc = static_cast<float *>(workspace);
+    float *crow = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((acc + 15) & ~(size_t)15));
+    return launch_bwd(*p, dq_acc, crow, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" const char *attn_last_error(void) { return g_msg; }
 
 extern "C" attn_status_t attn_device_error_flags(uint32_t *out, int32_t clear) {

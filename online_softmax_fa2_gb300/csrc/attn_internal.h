@@ -29,6 +29,8 @@ attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t 
 // Largest number of query rows per sequence the split-KV decode takes.
 constexpr int kMaxDecodeRows = 8;
 
+attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, cudaStream_t s);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -123,3 +123,29 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 4, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ofa.attn_fwd(q, q, q)
+
+
+def test_bwd_rejects_bad_arguments_on_the_host(lib):
+    def bp(**kw):
+        p = ofa.BwdParams()
+        p.fwd = _params(Nq=64, Nk=64, **kw)
+        p.fwd.lse = 0x60000
+        for name, addr in (("dout", 0x70000), ("dq", 0x80000), ("dk", 0x90000), ("dv", 0xA0000)):
+            setattr(p, name, addr)
+            setattr(p, name + "_stride", (ctypes.c_int64 * 3)(16 * 128, 128, 128))
+        return p
+    ws = ctypes.c_void_p(0xB0000)
+    need = lib.attn_bwd_workspace_bytes(1, 1, 64, 128)
+    assert need == 64 * 128 * 4 + 64 * 4
+    assert lib.attn_bwd(None, ws, need, None) == ofa.Status.INVALID_ARG
+    assert lib.attn_bwd(ctypes.byref(bp(dtype=0)), ws, need, None) == ofa.Status.UNSUPPORTED
+    assert lib.attn_bwd(ctypes.byref(bp(dk=192)), ws, need, None) == ofa.Status.UNSUPPORTED
+    assert lib.attn_bwd(ctypes.byref(bp()), ws, need - 4, None) == ofa.Status.WORKSPACE
+    assert lib.attn_bwd(ctypes.byref(bp()), None, need, None) == ofa.Status.WORKSPACE
+    p = bp()
+    p.fwd.lse = None
+    assert lib.attn_bwd(ctypes.byref(p), ws, need, None) == ofa.Status.INVALID_ARG
+    p = bp()
+    p.dq = 0x80004  # not 16-byte aligned
+    assert lib.attn_bwd(ctypes.byref(p), ws, need, None) == ofa.Status.MISALIGNED
+    assert lib.attn_bwd_workspace_bytes(-1, 1, 64, 128) == 0
