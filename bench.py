@@ -426,6 +426,8 @@ CASES = {
     "decode_nq4": ("decode", {"nq": 4, "causal": True}, "decode"),
     "decode_nq8": ("decode", {"nq": 8, "causal": True}, "decode"),
     "decode_nq4_b16": ("decode", {"B": 16, "nq": 4, "causal": True}, "decode"),
+    "bwd": ("causal_2k", {}, "bwd"),
+    "bwd_long": ("long_causal", {"H": 8}, "bwd"),
 }
 
 
@@ -446,6 +448,19 @@ def run_case(args):
         fn = lambda: ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
                                   scale=a.scale, out=o, lse=lse)
         work, unit = a.flops() / 1e12, "TFLOP/s"
+    elif kind == "bwd":
+        o, lse = ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
+                              scale=a.scale)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        dout = torch.randn(o.shape, generator=gen, device=dev).to(o.dtype)
+        ws = torch.empty(ofa.bwd_workspace_bytes(a.B, a.H, a.Nq, a.dk) // 4 + 4, dtype=torch.float32,
+                         device=dev)
+        dq, dk, dv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
+        fn = lambda: ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, bias=a.bias, kv_lens=a.kv_lens,
+                                  causal=a.causal, scale=a.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        # 2 (S) + 2 (dP) + 2 (dV) + 2 (dK) + 2 (dQ) products: (6 dk + 4 dv) FLOPs per visible pair
+        work, unit = a.visible_pairs() * (6 * a.dk + 4 * a.dv) / 1e12, "TFLOP/s"
     else:
         ws = torch.empty(ofa.decode_workspace_bytes(a.B, a.H, a.dv, a.num_splits, a.Nq) // 4,
                          dtype=torch.float32, device=dev)

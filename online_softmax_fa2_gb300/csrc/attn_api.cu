@@ -235,6 +235,8 @@ extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, s
         !stride_mult(f->o_stride, 8) || !stride_mult(p->dout_stride, 8) || !stride_mult(p->dq_stride, 8) ||
         !stride_mult(p->dk_stride, 8) || !stride_mult(p->dv_stride, 8))
         return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
+    if (f->B * f->Nq * f->H * (f->dk / 8) > INT32_MAX)
+        return fail(ATTN_ERR_UNSUPPORTED, "backward supports B * Nq * H * dk / 8 < 2^31");
     const size_t need = attn_bwd_workspace_bytes(f->B, f->H, f->Nq, f->dk);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)", need,

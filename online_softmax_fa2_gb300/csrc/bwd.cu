@@ -78,29 +78,36 @@ __device__ __forceinline__ int seq_n(const BwdArgs &a, int b, bool report) {
     return n;
 }
 
-// c_i = g_i . o_i and a zeroed dQ accumulator row; one warp per row (b * Nq + i) * H + h
+// c_i = g_i . o_i and a zeroed dQ accumulator row; D/8 lanes per row (b * Nq + i) * H + h,
+// each with 16-byte loads of o and g
 template <int D>
-__global__ void __launch_bounds__(128) bwd_prep_kernel(BwdArgs a) {
-    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= (long long)a.B * a.Nq * a.H) return;
-    const int h = (int)(row % a.H);
-    const long long bi = row / a.H;
-    const int i = (int)(bi % a.Nq), b = (int)(bi / a.Nq);
-    const __nv_bfloat16 *o = a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2;
-    const __nv_bfloat16 *g = a.g + b * a.gs0 + (long long)i * a.gs1 + h * a.gs2;
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
+    constexpr int LPR = D / 8;  // lanes per row
+    const int rows = a.B * a.Nq * a.H;
+    const int row = (blockIdx.x * 256 + threadIdx.x) / LPR, sub = threadIdx.x % LPR;
+    const bool live = row < rows;
     float acc = 0.f;
+    if (live) {
+        const int h = row % a.H, bi = row / a.H, i = bi % a.Nq, b = bi / a.Nq;
+        const uint4 ov = *reinterpret_cast<const uint4 *>(a.o + b * a.os0 + (long long)i * a.os1 + h * a.os2 + 8 * sub);
+        const uint4 gv = *reinterpret_cast<const uint4 *>(a.g + b * a.gs0 + (long long)i * a.gs1 + h * a.gs2 + 8 * sub);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-    for (int c = 2 * lane; c < D; c += 64) {
-        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + c));
-        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + c));
-        acc = fmaf(of.x, gf.x, fmaf(of.y, gf.y, acc));
+        for (int w = 0; w < 4; ++w) {
+            const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[w]));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[w]));
+            acc = fmaf(of.x, gf.x, fmaf(of.y, gf.y, acc));
+        }
+        float4 *dqa = reinterpret_cast<float4 *>(a.dq_acc + (long long)row * D + 8 * sub);
+        dqa[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dqa[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) a.crow[((long long)b * a.H + h) * a.Nq + i] = acc;
-    float4 *dqa = reinterpret_cast<float4 *>(a.dq_acc + row * D);
-    if (lane < D / 4) dqa[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && sub == 0) {
+        const int h = row % a.H, bi = row / a.H, i = bi % a.Nq, b = bi / a.Nq;
+        a.crow[((long long)b * a.H + h) * a.Nq + i] = acc;
+    }
 }
 
 template <int D>
@@ -330,20 +337,18 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_main_kernel(BwdArgs a) {
     }
 }
 
-// dQ accumulator (fp32 [B, Nq, H, D]) -> bf16 dQ with the caller's strides
+// dQ accumulator (fp32 [B, Nq, H, D]) -> bf16 dQ with the caller's strides; 8 values per
+// thread (two 16-byte loads, one 16-byte store)
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a) {
-    const long long total = (long long)a.B * a.Nq * a.H * (D / 2);
-    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
-         x += (long long)gridDim.x * blockDim.x) {
-        const long long row = x / (D / 2);
-        const int c = 2 * (int)(x % (D / 2));
-        const int h = (int)(row % a.H);
-        const long long bi = row / a.H;
-        const int i = (int)(bi % a.Nq), b = (int)(bi / a.Nq);
-        const float2 f = *reinterpret_cast<const float2 *>(a.dq_acc + row * D + c);
-        *reinterpret_cast<uint32_t *>(a.dq + b * a.dqs0 + (long long)i * a.dqs1 + h * a.dqs2 + c) = pack_bf16(f.x, f.y);
-    }
+    const int rows = a.B * a.Nq * a.H;
+    const int x = blockIdx.x * 256 + threadIdx.x, row = x / (D / 8), c = 8 * (x % (D / 8));
+    if (row >= rows) return;
+    const int h = row % a.H, bi = row / a.H, i = bi % a.Nq, b = bi / a.Nq;
+    const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc + (long long)row * D + c);
+    const float4 f0 = src[0], f1 = src[1];
+    *reinterpret_cast<uint4 *>(a.dq + b * a.dqs0 + (long long)i * a.dqs1 + h * a.dqs2 + c) =
+        make_uint4(pack_bf16(f0.x, f0.y), pack_bf16(f0.z, f0.w), pack_bf16(f1.x, f1.y), pack_bf16(f1.z, f1.w));
 }
 
 template <int D, bool kBias>
@@ -359,8 +364,9 @@ cudaError_t launch_main(const BwdArgs &a, cudaStream_t st) {
 template <int D>
 cudaError_t launch_all(const BwdArgs &a, cudaStream_t st) {
     const long long rows = (long long)a.B * a.Nq * a.H;
+    const unsigned row_blocks = (unsigned)((rows * (D / 8) + 255) / 256);
     if (rows > 0) {
-        bwd_prep_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(a);
+        bwd_prep_kernel<D><<<row_blocks, 256, 0, st>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -369,9 +375,7 @@ cudaError_t launch_all(const BwdArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     if (rows > 0) {
-        const long long total = rows * (D / 2);
-        const long long blocks = (total + 255) / 256;
-        bwd_dq_kernel<D><<<(unsigned)(blocks < 65536 ? blocks : 65536), 256, 0, st>>>(a);
+        bwd_dq_kernel<D><<<row_blocks, 256, 0, st>>>(a);
         return cudaGetLastError();
     }
     return cudaSuccess;
