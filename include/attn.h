@@ -19,9 +19,10 @@
  *       section 5  tile loop, rows keep their own state, divide once at the end;
  *       section 6  global positions; causal masks align the two sequences' ends
  *                  ("bottom-right"); an entirely empty row returns zero;
- *       section 7  the saved log-sum-exp L_i;
- *       section 8  decode (one query row, a long key/value cache) split over the keys,
- *                  the partial states merged.
+ *       section 7  the saved log-sum-exp L_i, and the backward that rebuilds the
+ *                  probabilities from it (attn_bwd);
+ *       section 8  decode (one query row, or a few, against a long key/value cache) split
+ *                  over the keys, the partial states merged.
  *   "Flash attention and efficient attention: Visual walkthrough", Steps 4-5 (the three
  *       running numbers; re-basing a sum to a new maximum by one multiply).
  *   "Reducing Memory Traffic with Output Accumulation in FlashAttention", Figures 1-3
