@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn_gb300.so")
 SOURCES = ["attn_api.cu", "fwd_f32.cu", "fwd_bf16_sm103.cu", "fwd_bf16_pair_sm103.cu", "decode.cu",
-           "bwd.cu"]
+           "bwd.cu", "bwd_tc_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", os.path.join(HERE, "..", "include")]

@@ -1,6 +1,7 @@
 // attn_internal.h -- host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,6 +31,15 @@ attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t 
 constexpr int kMaxDecodeRows = 8;
 
 attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, cudaStream_t s);
+
+// 4-D TMA map over a bf16 [B, N, H, d] tensor with element strides s (b, n, h); box 64 x 128,
+// 128-byte swizzle (fwd_bf16_sm103.cu).
+attn_status_t encode(CUtensorMap *m, const void *ptr, int64_t B, int64_t N, int64_t H, int64_t d,
+                     const int64_t s[3], const char *name);
+
+// Backward of dk == dv == 128 without a bias on the tcgen05 tensor cores (bwd_tc_sm103.cu);
+// dq_acc and crow as for launch_bwd, already filled by the prep kernel.
+attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -9,7 +9,8 @@
 // dV_j += p_ij g_i, dK_j += scale dS_ij q_i, dQ_i += scale dS_ij k_j, and discards the tile.
 // The bias is fixed (no gradient is formed for it); an empty row passes no gradient.
 //
-// Three kernels on the caller's stream:
+// Three kernels on the caller's stream (with dk == dv == 128 and no bias the products run in
+// bwd_tc_sm103.cu's tcgen05 kernel instead of bwd_main_kernel):
 //   bwd_prep_kernel   c_i = g_i . o_i per row (fp32, into the workspace) and a zeroed fp32 dQ
 //                     accumulator row;
 //   bwd_main_kernel   one CTA per (64-key block, h, b), four warps, warp w owning keys
@@ -361,8 +362,11 @@ cudaError_t launch_main(const BwdArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// Prep, then the products (the tcgen05 kernel for d = 128 without a bias, the warp-level
+// kernel otherwise), then the dQ conversion.  A failed tcgen05 launch reports through
+// attn_last_error and returns cudaErrorLaunchFailure here.
 template <int D>
-cudaError_t launch_all(const BwdArgs &a, cudaStream_t st) {
+cudaError_t launch_all(const BwdArgs &a, const attn_bwd_params_t &p, cudaStream_t st) {
     const long long rows = (long long)a.B * a.Nq * a.H;
     const unsigned row_blocks = (unsigned)((rows * (D / 8) + 255) / 256);
     if (rows > 0) {
@@ -371,8 +375,12 @@ cudaError_t launch_all(const BwdArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     if ((long long)a.B * a.H * a.Nk > 0) {
-        cudaError_t e = a.bias ? launch_main<D, true>(a, st) : launch_main<D, false>(a, st);
-        if (e != cudaSuccess) return e;
+        if (D == 128 && !a.bias) {
+            if (launch_bwd_tc(p, a.dq_acc, a.crow, st) != ATTN_OK) return cudaErrorLaunchFailure;
+        } else {
+            cudaError_t e = a.bias ? launch_main<D, true>(a, st) : launch_main<D, false>(a, st);
+            if (e != cudaSuccess) return e;
+        }
     }
     if (rows > 0) {
         bwd_dq_kernel<D><<<row_blocks, 256, 0, st>>>(a);
@@ -411,7 +419,8 @@ attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow,
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     if (f.B > 65535 || f.H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "backward supports B, H <= 65535");
-    const cudaError_t e = f.dk == 64 ? launch_all<64>(a, st) : launch_all<128>(a, st);
+    const cudaError_t e = f.dk == 64 ? launch_all<64>(a, p, st) : launch_all<128>(a, p, st);
+    if (e == cudaErrorLaunchFailure && attn_last_error()[0]) return ATTN_ERR_CUDA;  // message set by the tcgen05 launcher
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }

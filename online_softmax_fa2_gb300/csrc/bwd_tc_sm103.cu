@@ -1,0 +1,419 @@
+// bwd_tc_sm103.cu -- attention backward for dk == dv == 128 (no bias) on the 5th-generation
+// tensor cores.
+//
+// The same gradients as bwd.cu ("How Does FlashAttention Preserve Global Softmax Across
+// Tiles?", section 7: rebuild p_ij = exp(x_ij - L_i), c_i = g_i . o_i, dS_ij = p_ij (g_i . v_j -
+// c_i); dV_j += p_ij g_i, dK_j += scale dS_ij q_i, dQ_i += scale dS_ij k_j), with 128 x 128 tiles
+// whose five products run as tcgen05.mma into tensor memory.  One CTA owns a block of 128 keys
+// of one (b, h) and walks the query tiles of 128 rows that see any of its keys:
+//
+//   TMEM (512 columns)   S^T / P^T [0, 128)   dP^T / dS^T [128, 256)   dV [256, 384)   dK [384, 512)
+//                        dQ of the tile goes into [128, 256) once dS^T has been read there, so
+//                        the next tile's S^T can start while dQ is read out.
+//   S^T  = K Q^T         A = K, B = Q   (both [row][dim] in shared memory, K-major)
+//   dP^T = V G^T         A = V, B = G   (G: the upstream gradient dL/dO)
+//   P^T, dS^T            one thread per key (TMEM lane): mask, exp(x - L), (dP - c); P^T and
+//                        dS^T go back into TMEM as bf16, dS^T also into shared memory
+//   dV  += P^T G         A = P^T from TMEM, B = G read MN-major (as V in the forward's P V)
+//   dK  += dS^T Q        A = dS^T from TMEM, B = Q read MN-major
+//   dQ   = dS K          A = dS read MN-major from the [key][row] copy, B = K read MN-major
+//
+// Roles (384 threads): warp 0 loads K and V once and Q, G per tile with TMA; warp 1 issues the
+// products (one thread); warps 4-7 form P^T and dS^T and, at the end, write dK (times scale)
+// and dV; warps 8-11 read each tile's dQ from TMEM (one thread per row) and add scale * dQ to
+// the fp32 accumulator with vector reductions.  Every mbarrier wait is bounded as in the
+// forward kernels.
+#include "fwd_bf16_common.cuh"
+
+namespace attn {
+namespace {
+
+using namespace bf16fwd;
+
+constexpr int kTcThreads = 384;
+constexpr int kTile = 2 * kPanelBytes;  // 128 rows x 128 bf16: two 64-column 128B-swizzled panels
+// K, V, then Q and G in two stages each, then the [key][row] copy of dS^T
+constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffG = 4 * kTile, kOffS = 6 * kTile;
+constexpr int kOffCtrl = 7 * kTile;
+
+struct TcArgs {
+    int B, H, Nq, Nk, causal;
+    float scale, scale_log2;
+    const float *lse, *crow;  // [B, H, Nq]
+    const int *kv_lens;
+    float *dq_acc;  // [B, Nq, H, 128]
+    __nv_bfloat16 *dk, *dv;
+    long long dks0, dks1, dks2, dvs0, dvs1, dvs2;
+    uint32_t *flags;
+};
+
+struct TcCtrl {
+    uint64_t kv_full, q_full[2], q_empty[2], s_full, p_ready, dq_full, dq_free, ds_free, kv_final;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr int kSmemBytes = kOffCtrl + (int)sizeof(TcCtrl) + 1024;
+static_assert(kSmemBytes <= kSmemMax, "shared memory budget");
+
+// kind::f16 instruction descriptor with bf16 A and B, fp32 D, A and B K-major or MN-major
+// (bit 15: A MN-major, bit 16: B MN-major)
+__host__ __device__ constexpr uint32_t idesc_ab(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                  const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    TcCtrl *ctrl = reinterpret_cast<TcCtrl *>(smem + kOffCtrl);
+    volatile int *abort = &ctrl->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+
+    int n = a.Nk;
+    if (a.kv_lens) {
+        const int raw = a.kv_lens[b];
+        n = min(max(raw, 0), a.Nk);
+        if (raw != n && threadIdx.x == 0 && kb == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
+    }
+    const int shift = n - a.Nq;  // causal: key j visible to row i iff j <= i + shift
+    const int j0 = kb * BK;
+    const int i_first = a.causal ? max(0, j0 - shift) : 0;
+    const bool any = j0 < n && i_first < a.Nq;
+    const int t_first = i_first / BQ, t_end = any ? (a.Nq + BQ - 1) / BQ : t_first;
+
+    if (!any) {  // no row sees a key of this block: dK = dV = 0
+        if (warp >= 4 && warp < 8) {
+            const int j = j0 + (int)threadIdx.x - 128;
+            if (j < a.Nk) {
+                uint4 *dkr = reinterpret_cast<uint4 *>(a.dk + b * a.dks0 + (long long)j * a.dks1 + h * a.dks2);
+                uint4 *dvr = reinterpret_cast<uint4 *>(a.dv + b * a.dvs0 + (long long)j * a.dvs1 + h * a.dvs2);
+                for (int c = 0; c < 16; ++c) dkr[c] = dvr[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&ctrl->kv_full, 1);
+        for (int st = 0; st < 2; ++st) {
+            ptx::mbar_init(&ctrl->q_full[st], 1);
+            ptx::mbar_init(&ctrl->q_empty[st], 1);
+        }
+        ptx::mbar_init(&ctrl->s_full, 1);
+        ptx::mbar_init(&ctrl->p_ready, 128);
+        ptx::mbar_init(&ctrl->dq_full, 1);
+        ptx::mbar_init(&ctrl->dq_free, 128);
+        ptx::mbar_init(&ctrl->ds_free, 1);
+        ptx::mbar_init(&ctrl->kv_final, 1);
+        ctrl->abort = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_g);
+        ptx::mbar_arrive_expect_tx(&ctrl->kv_full, 2 * kTile);
+        for (int p = 0; p < 2; ++p) {
+            ptx::tma_load_4d(smem + kOffK + p * kPanelBytes, &tm_k, &ctrl->kv_full, p * 64, j0, h, b);
+            ptx::tma_load_4d(smem + kOffV + p * kPanelBytes, &tm_v, &ctrl->kv_full, p * 64, j0, h, b);
+        }
+        ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], 2 * kTile);
+        for (int p = 0; p < 2; ++p) {
+            ptx::tma_load_4d(smem + kOffQ + p * kPanelBytes, &tm_q, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
+            ptx::tma_load_4d(smem + kOffG + p * kPanelBytes, &tm_g, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
+        }
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&ctrl->tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        return ptx::mbar_wait(bar, parity, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
+    };
+    const int ntiles = t_end - t_first;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int loaded = 1;
+            // tile k into stage k & 1, once the products of tile k - 2 have read that stage
+            for (int k = 1; k < ntiles; ++k) {
+                const int st = k & 1;
+                if (k >= 2 && !wait(&ctrl->q_empty[st], ((k >> 1) - 1) & 1)) break;
+                const int i0 = (t_first + k) * BQ;
+                ptx::mbar_arrive_expect_tx(&ctrl->q_full[st], 2 * kTile);
+                for (int p = 0; p < 2; ++p) {
+                    ptx::tma_load_4d(smem + kOffQ + st * kTile + p * kPanelBytes, &tm_q, &ctrl->q_full[st], p * 64, i0,
+                                     h, b);
+                    ptx::tma_load_4d(smem + kOffG + st * kTile + p * kPanelBytes, &tm_g, &ctrl->q_full[st], p * 64, i0,
+                                     h, b);
+                }
+                ++loaded;
+            }
+            if (*abort) {  // copies in flight land before the CTA exits
+                ptx::mbar_wait_quiet(&ctrl->kv_full, 0, kWaitLimitNs);
+                for (int k = max(0, loaded - 2); k < loaded; ++k)
+                    ptx::mbar_wait_quiet(&ctrl->q_full[k & 1], (k >> 1) & 1, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ tensor-core issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_ab(BQ, BK, false, false);  // S^T, dP^T
+            constexpr uint32_t kIdKV = idesc_ab(BQ, 128, false, true);  // dV, dK: A from TMEM, B MN-major
+            constexpr uint32_t kIdQ = idesc_ab(BQ, 128, true, true);    // dQ: A and B MN-major
+            const uint32_t sK = ptx::smem_u32(smem + kOffK), sV = ptx::smem_u32(smem + kOffV);
+            const uint32_t sS = ptx::smem_u32(smem + kOffS);
+            bool ok = wait(&ctrl->kv_full, 0);
+            for (int k = 0; ok && k < ntiles; ++k) {
+                const int st = k & 1;
+                const uint32_t sQ = ptx::smem_u32(smem + kOffQ + st * kTile), sG = ptx::smem_u32(smem + kOffG + st * kTile);
+                if (!wait(&ctrl->q_full[st], (k >> 1) & 1)) break;
+                ptx::tc_fence_after();
+                {
+                    // K-major operands: 16-dim steps are 32 bytes apart inside a 64-column panel
+                    const uint64_t kd = ptx::sdesc_sw128(sK, 16, 1024), qd = ptx::sdesc_sw128(sQ, 16, 1024);
+                    const uint64_t vd = ptx::sdesc_sw128(sV, 16, 1024), gd = ptx::sdesc_sw128(sG, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
+                        ptx::mma_ss(tmem + 0, kd + off, qd + off, kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    // dP^T goes where the previous tile's dQ was: wait until it has been read
+                    if (k > 0 && !wait(&ctrl->dq_free, (k - 1) & 1)) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
+                        ptx::mma_ss(tmem + 128, vd + off, gd + off, kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&ctrl->s_full);
+                }
+                if (!wait(&ctrl->p_ready, k & 1)) break;
+                ptx::tc_fence_after();
+                {
+                    // MN-major operands: 16-row steps are 16 rows x 128 bytes apart; the two
+                    // 64-wide panels of the N (or M) dimension are kPanelBytes apart
+                    const uint64_t gm = ptx::sdesc_sw128(sG, kPanelBytes, 1024);
+                    const uint64_t qm = ptx::sdesc_sw128(sQ, kPanelBytes, 1024);
+                    const uint64_t km = ptx::sdesc_sw128(sK, kPanelBytes, 1024);
+                    const uint64_t sm_ = ptx::sdesc_sw128(sS, kPanelBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dV += P^T G: P^T bf16 pairs, 8 columns per 16 rows
+                        ptx::mma_ts(tmem + 256, tmem + 0 + kk * 8, gm + ((kk * 16 * 128) >> 4), kIdKV,
+                                    (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
+                        ptx::mma_ts(tmem + 384, tmem + 128 + kk * 8, qm + ((kk * 16 * 128) >> 4), kIdKV,
+                                    (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dQ = dS K into the columns dS^T occupied
+                        ptx::mma_ss(tmem + 128, sm_ + ((kk * 16 * 128) >> 4), km + ((kk * 16 * 128) >> 4), kIdQ,
+                                    kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(&ctrl->dq_full);
+                    ptx::mma_commit(&ctrl->ds_free);
+                    ptx::mma_commit(&ctrl->q_empty[st]);
+                }
+            }
+            ptx::mma_commit(&ctrl->kv_final);
+            if (!ptx::mbar_wait_quiet(&ctrl->kv_final, 0, kWaitLimitNs)) atomicOr(a.flags, kFlagWaitTimeout);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P^T and dS^T (one key each)
+        const int r = (int)threadIdx.x - 128;  // key in the block == TMEM lane
+        const int j = j0 + r;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        auto wait_warp = [&](uint64_t *bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait(bar, parity));
+        };
+        bool ok = wait_warp(&ctrl->kv_full, 0);
+        if (ok && j >= n) {  // K rows past the sequence may hold anything: zero them for dQ = dS K
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                uint4 *dst = reinterpret_cast<uint4 *>(smem + kOffK + p * kPanelBytes + r * 128);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) dst[t] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        const float *lse_bh = a.lse + ((long long)b * a.H + h) * a.Nq;
+        const float *c_bh = a.crow + ((long long)b * a.H + h) * a.Nq;
+        for (int k = 0; ok && k < ntiles; ++k) {
+            const int i0 = (t_first + k) * BQ;
+            if (!wait_warp(&ctrl->s_full, k & 1) || (k > 0 && !wait_warp(&ctrl->ds_free, (k - 1) & 1))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {  // rows 32c .. 32c + 31 of the tile
+                // L and c of these rows: lane t loads row 32c + t; row 32c + e is then lane e's
+                const int it = i0 + 32 * c + lane;
+                const float Lt = it < a.Nq ? __ldg(lse_bh + it) * kLog2e : 0.f;
+                const float Ct = it < a.Nq ? __ldg(c_bh + it) : 0.f;
+                uint32_t sv[32], dv[32];
+                ptx::tmem_ld32(lane_addr + 32 * c, sv);
+                ptx::tmem_ld32(lane_addr + 128 + 32 * c, dv);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(sv);
+                ptx::reg_fence(dv);
+                uint32_t pp[16], dp[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pe[2], de[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = i0 + 32 * c + e + u;
+                        const bool vis = j < n && i < a.Nq && (!a.causal || j <= i + shift);
+                        const float Li = __shfl_sync(0xffffffffu, Lt, e + u);
+                        const float Ci = __shfl_sync(0xffffffffu, Ct, e + u);
+                        const float p = vis ? ptx::ex2(__uint_as_float(sv[e + u]) * a.scale_log2 - Li) : 0.f;
+                        pe[u] = p;
+                        // a select, not a product: dP^T of a key past the sequence may be NaN
+                        de[u] = vis ? p * (__uint_as_float(dv[e + u]) - Ci) : 0.f;
+                    }
+                    pp[e / 2] = ptx::pack_bf16x2(pe[0], pe[1]);
+                    dp[e / 2] = ptx::pack_bf16x2(de[0], de[1]);
+                }
+                tmem_st16(lane_addr + 16 * c, pp);        // P^T over the S^T columns already read
+                tmem_st16(lane_addr + 128 + 16 * c, dp);  // dS^T over the dP^T columns already read
+                // dS^T into shared memory as [key][row]: rows 32c.. are 16-byte chunks
+                // 4 (c % 2) .. + 3 of panel c / 2, 128-byte swizzled like a TMA box
+                uint8_t *row = smem + kOffS + (c / 2) * kPanelBytes + r * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = (c % 2) * 4 + q;
+                    *reinterpret_cast<uint4 *>(row + ((chunk ^ (r & 7)) * 16)) =
+                        make_uint4(dp[4 * q], dp[4 * q + 1], dp[4 * q + 2], dp[4 * q + 3]);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&ctrl->p_ready);
+        }
+        // dK (times scale) and dV of this key
+        if (ok && wait_warp(&ctrl->kv_final, 0)) {
+            ptx::tc_fence_after();
+            __nv_bfloat16 *dkr = a.dk + b * a.dks0 + (long long)j * a.dks1 + h * a.dks2;
+            __nv_bfloat16 *dvr = a.dv + b * a.dvs0 + (long long)j * a.dvs1 + h * a.dvs2;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t kv[32], vv[32];
+                ptx::tmem_ld32(lane_addr + 384 + 32 * c, kv);
+                ptx::tmem_ld32(lane_addr + 256 + 32 * c, vv);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(kv);
+                ptx::reg_fence(vv);
+                if (j < a.Nk) {
+                    const bool seen = j < n;  // a key past the sequence gets +0.0 exactly
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t pk[4], pv[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            pk[t] = ptx::pack_bf16x2(a.scale * __uint_as_float(kv[8 * q + 2 * t]),
+                                                     a.scale * __uint_as_float(kv[8 * q + 2 * t + 1]));
+                            pv[t] = ptx::pack_bf16x2(__uint_as_float(vv[8 * q + 2 * t]), __uint_as_float(vv[8 * q + 2 * t + 1]));
+                        }
+                        *reinterpret_cast<uint4 *>(dkr + 32 * c + 8 * q) =
+                            seen ? make_uint4(pk[0], pk[1], pk[2], pk[3]) : make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(dvr + 32 * c + 8 * q) =
+                            seen ? make_uint4(pv[0], pv[1], pv[2], pv[3]) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ (one query row each)
+        const int r = (int)threadIdx.x - 256;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        for (int k = 0; k < ntiles; ++k) {
+            const bool w = ptx::mbar_wait(&ctrl->dq_full, k & 1, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, w)) break;
+            ptx::tc_fence_after();
+            const int i = (t_first + k) * BQ + r;
+            float *dst = a.dq_acc + (((long long)b * a.Nq + i) * a.H + h) * 128;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t qv[32];
+                ptx::tmem_ld32(lane_addr + 128 + 32 * c, qv);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(qv);
+                if (i < a.Nq) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        red_add_v4(dst + 32 * c + 4 * q, a.scale * __uint_as_float(qv[4 * q]),
+                                   a.scale * __uint_as_float(qv[4 * q + 1]), a.scale * __uint_as_float(qv[4 * q + 2]),
+                                   a.scale * __uint_as_float(qv[4 * q + 3]));
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&ctrl->dq_free);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, cudaStream_t s) {
+    const attn_fwd_params_t &f = p.fwd;
+    CUtensorMap mq, mk, mv, mg;
+    attn_status_t st;
+    if ((st = encode(&mq, f.q, f.B, f.Nq, f.H, 128, f.q_stride, "q")) ||
+        (st = encode(&mk, f.k, f.B, f.Nk, f.H, 128, f.k_stride, "k")) ||
+        (st = encode(&mv, f.v, f.B, f.Nk, f.H, 128, f.v_stride, "v")) ||
+        (st = encode(&mg, p.dout, f.B, f.Nq, f.H, 128, p.dout_stride, "dout")))
+        return st;
+    TcArgs a;
+    a.B = (int)f.B; a.H = (int)f.H; a.Nq = (int)f.Nq; a.Nk = (int)f.Nk; a.causal = f.causal;
+    a.scale = f.scale; a.scale_log2 = f.scale * kLog2e;
+    a.lse = f.lse; a.crow = crow; a.kv_lens = f.kv_lens; a.dq_acc = dq_acc;
+    a.dk = static_cast<__nv_bfloat16 *>(p.dk);
+    a.dv = static_cast<__nv_bfloat16 *>(p.dv);
+    a.dks0 = p.dk_stride[0]; a.dks1 = p.dk_stride[1]; a.dks2 = p.dk_stride[2];
+    a.dvs0 = p.dv_stride[0]; a.dvs1 = p.dv_stride[1]; a.dvs2 = p.dv_stride[2];
+    a.flags = device_flags();
+    if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    dim3 grid((unsigned)((f.Nk + BK - 1) / BK), (unsigned)f.H, (unsigned)f.B);
+    bwd_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(mq, mk, mv, mg, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward (tcgen05) launch: %s", cudaGetErrorString(e));
+    return ATTN_OK;
+}
+
+}  // namespace attn

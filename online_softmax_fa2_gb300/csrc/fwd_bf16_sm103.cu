@@ -447,6 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------- host side
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -479,6 +481,8 @@ attn_status_t encode(CUtensorMap *m, const void *ptr, int64_t B, int64_t N, int6
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "TMA descriptor for %s rejected (CUresult %d)", name, (int)r);
     return ATTN_OK;
 }
+
+namespace {
 
 // 4-D map over the fp32 bias [B, H, Nq, Nk] (key stride 1, element strides bs: b, h, i);
 // box 32 keys x 128 rows, 128-byte swizzle.  Returns false when the bias does not meet the
