@@ -202,11 +202,22 @@ extern "C" attn_status_t attn_merge_states(const float *partials, int64_t B, int
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk) {
-    if (B < 0 || H < 0 || Nq < 0 || dk < 1) return 0;
+// dQ accumulator [B, Nq, H, dk], c_i [B, H, Nq], and lse * log2 e [B, H, Nq rounded up to 128]
+// (whole 128-row tiles of it are copied with one bulk copy each), each 16-byte aligned.
+static size_t bwd_ws_parts(int64_t B, int64_t H, int64_t Nq, int64_t dk, size_t *off_c, size_t *off_l) {
+    auto up16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
     const size_t acc = (size_t)B * (size_t)H * (size_t)Nq * (size_t)dk * sizeof(float);
     const size_t rows = (size_t)B * (size_t)H * (size_t)Nq * sizeof(float);
-    return ((acc + 15) & ~(size_t)15) + rows;
+    const size_t padded = (size_t)B * (size_t)H * (size_t)((Nq + 127) / 128 * 128) * sizeof(float);
+    *off_c = up16(acc);
+    *off_l = *off_c + up16(rows);
+    return *off_l + padded;
+}
+
+extern "C" size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk) {
+    if (B < 0 || H < 0 || Nq < 0 || dk < 1) return 0;
+    size_t oc, ol;
+    return bwd_ws_parts(B, H, Nq, dk, &oc, &ol);
 }
 
 extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, size_t workspace_bytes,
@@ -241,10 +252,12 @@ extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, s
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)", need,
                     workspace_bytes);
-    const size_t acc = (size_t)f->B * f->H * f->Nq * f->dk * sizeof(float);
+    size_t off_c, off_l;
+    bwd_ws_parts(f->B, f->H, f->Nq, f->dk, &off_c, &off_l);
     float *dq_acc = static_cast<float *>(workspace);
-    float *crow = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((acc + 15) & ~(size_t)15));
-    return launch_bwd(*p, dq_acc, crow, reinterpret_cast<cudaStream_t>(stream));
+    float *crow = reinterpret_cast<float *>(static_cast<char *>(workspace) + off_c);
+    float *lrow = reinterpret_cast<float *>(static_cast<char *>(workspace) + off_l);
+    return launch_bwd(*p, dq_acc, crow, lrow, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" const char *attn_last_error(void) { return g_msg; }

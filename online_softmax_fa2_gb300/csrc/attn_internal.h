@@ -30,7 +30,7 @@ attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t 
 // Largest number of query rows per sequence the split-KV decode takes.
 constexpr int kMaxDecodeRows = 8;
 
-attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, cudaStream_t s);
+attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, float *lrow, cudaStream_t s);
 
 // 4-D TMA map over a bf16 [B, N, H, d] tensor with element strides s (b, n, h); box 64 x 128,
 // 128-byte swizzle (fwd_bf16_sm103.cu).
@@ -38,8 +38,10 @@ attn_status_t encode(CUtensorMap *m, const void *ptr, int64_t B, int64_t N, int6
                      const int64_t s[3], const char *name);
 
 // Backward of dk == dv == 128 without a bias on the tcgen05 tensor cores (bwd_tc_sm103.cu);
-// dq_acc and crow as for launch_bwd, already filled by the prep kernel.
-attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, cudaStream_t s);
+// dq_acc, crow and lrow (lse * log2 e, rows padded to a multiple of 128) as for launch_bwd,
+// already filled by the prep kernel.
+attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, const float *lrow,
+                            cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

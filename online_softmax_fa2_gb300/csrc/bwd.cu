@@ -60,6 +60,7 @@ struct BwdArgs {
     const int *kv_lens;
     float *dq_acc;  // [B, Nq, H, D] fp32
     float *crow;    // [B, H, Nq] fp32: c_i = g_i . o_i
+    float *lrow;    // [B, H, Nq rounded up to 128] fp32: lse_i * log2 e
     __nv_bfloat16 *dq, *dk, *dv;
     long long dqs0, dqs1, dqs2, dks0, dks1, dks2, dvs0, dvs1, dvs2;
     uint32_t *flags;
@@ -108,6 +109,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
     if (live && sub == 0) {
         const int h = row % a.H, bi = row / a.H, i = bi % a.Nq, b = bi / a.Nq;
         a.crow[((long long)b * a.H + h) * a.Nq + i] = acc;
+        const int nq_pad = (a.Nq + 127) / 128 * 128;
+        a.lrow[((long long)b * a.H + h) * nq_pad + i] = a.lse[((long long)b * a.H + h) * a.Nq + i] * kLog2e;
     }
 }
 
@@ -376,7 +379,7 @@ cudaError_t launch_all(const BwdArgs &a, const attn_bwd_params_t &p, cudaStream_
     }
     if ((long long)a.B * a.H * a.Nk > 0) {
         if (D == 128 && !a.bias) {
-            if (launch_bwd_tc(p, a.dq_acc, a.crow, st) != ATTN_OK) return cudaErrorLaunchFailure;
+            if (launch_bwd_tc(p, a.dq_acc, a.crow, a.lrow, st) != ATTN_OK) return cudaErrorLaunchFailure;
         } else {
             cudaError_t e = a.bias ? launch_main<D, true>(a, st) : launch_main<D, false>(a, st);
             if (e != cudaSuccess) return e;
@@ -391,7 +394,7 @@ cudaError_t launch_all(const BwdArgs &a, const attn_bwd_params_t &p, cudaStream_
 
 }  // namespace
 
-attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, cudaStream_t st) {
+attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, float *lrow, cudaStream_t st) {
     const attn_fwd_params_t &f = p.fwd;
     BwdArgs a;
     a.B = (int)f.B; a.H = (int)f.H; a.Nq = (int)f.Nq; a.Nk = (int)f.Nk; a.causal = f.causal;
@@ -409,7 +412,7 @@ attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow,
     a.lse = f.lse;
     a.bias = f.bias; a.bs0 = f.bias_stride[0]; a.bs1 = f.bias_stride[1]; a.bs2 = f.bias_stride[2];
     a.kv_lens = f.kv_lens;
-    a.dq_acc = dq_acc; a.crow = crow;
+    a.dq_acc = dq_acc; a.crow = crow; a.lrow = lrow;
     a.dq = static_cast<__nv_bfloat16 *>(p.dq);
     a.dk = static_cast<__nv_bfloat16 *>(p.dk);
     a.dv = static_cast<__nv_bfloat16 *>(p.dv);

@@ -34,12 +34,15 @@ constexpr int kTcThreads = 384;
 constexpr int kTile = 2 * kPanelBytes;  // 128 rows x 128 bf16: two 64-column 128B-swizzled panels
 // K, V, then Q and G in two stages each, then the [key][row] copy of dS^T
 constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffG = 4 * kTile, kOffS = 6 * kTile;
-constexpr int kOffCtrl = 7 * kTile;
+constexpr int kOffL = 7 * kTile;         // lse * log2 e of the tile's 128 rows, two stages
+constexpr int kOffCtrl = kOffL + 2 * 512;
 
 struct TcArgs {
     int B, H, Nq, Nk, causal;
     float scale, scale_log2;
-    const float *lse, *crow;  // [B, H, Nq]
+    const float *crow;  // [B, H, Nq]
+    const float *lrow;  // [B, H, nq_pad]: lse * log2 e, rows padded to a multiple of 128
+    int nq_pad;
     const int *kv_lens;
     float *dq_acc;  // [B, Nq, H, 128]
     __nv_bfloat16 *dk, *dv;
@@ -63,6 +66,15 @@ __host__ __device__ constexpr uint32_t idesc_ab(int M, int N, bool a_mn, bool b_
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte aligned),
+// completion counted on `bar`
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     ptx::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(ptx::smem_u32(bar))
+                 : "memory");
+}
+
 // 32 lanes x 32 bits, 16 consecutive columns
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -72,6 +84,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+
+}  // namespace
+namespace ptx {
+// (d0, d1) = (a0 * b0, a1 * b1) in one packed instruction
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+}  // namespace ptx
+namespace {
 
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -137,7 +161,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ptx::tma_load_4d(smem + kOffK + p * kPanelBytes, &tm_k, &ctrl->kv_full, p * 64, j0, h, b);
             ptx::tma_load_4d(smem + kOffV + p * kPanelBytes, &tm_v, &ctrl->kv_full, p * 64, j0, h, b);
         }
-        ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], 2 * kTile);
+        ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], 2 * kTile + 512);
+        bulk_load(smem + kOffL, a.lrow + ((long long)b * a.H + h) * a.nq_pad + t_first * BQ, 512, &ctrl->q_full[0]);
         for (int p = 0; p < 2; ++p) {
             ptx::tma_load_4d(smem + kOffQ + p * kPanelBytes, &tm_q, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
             ptx::tma_load_4d(smem + kOffG + p * kPanelBytes, &tm_g, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
@@ -165,7 +190,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int st = k & 1;
                 if (k >= 2 && !wait(&ctrl->q_empty[st], ((k >> 1) - 1) & 1)) break;
                 const int i0 = (t_first + k) * BQ;
-                ptx::mbar_arrive_expect_tx(&ctrl->q_full[st], 2 * kTile);
+                ptx::mbar_arrive_expect_tx(&ctrl->q_full[st], 2 * kTile + 512);
+                bulk_load(smem + kOffL + st * 512, a.lrow + ((long long)b * a.H + h) * a.nq_pad + i0, 512,
+                          &ctrl->q_full[st]);
                 for (int p = 0; p < 2; ++p) {
                     ptx::tma_load_4d(smem + kOffQ + st * kTile + p * kPanelBytes, &tm_q, &ctrl->q_full[st], p * 64, i0,
                                      h, b);
@@ -260,21 +287,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         ptx::fence_proxy_async_smem();
-        const float *lse_bh = a.lse + ((long long)b * a.H + h) * a.Nq;
         const float *c_bh = a.crow + ((long long)b * a.H + h) * a.Nq;
         for (int k = 0; ok && k < ntiles; ++k) {
             const int i0 = (t_first + k) * BQ;
-            if (!wait_warp(&ctrl->s_full, k & 1) || (k > 0 && !wait_warp(&ctrl->ds_free, (k - 1) & 1))) {
+            // s_full implies the tile's copies are done; waiting on their barrier as well makes
+            // the copied L visible to these threads
+            if (!wait_warp(&ctrl->s_full, k & 1) || !wait_warp(&ctrl->q_full[k & 1], (k >> 1) & 1) ||
+                (k > 0 && !wait_warp(&ctrl->ds_free, (k - 1) & 1))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {  // rows 32c .. 32c + 31 of the tile
-                // L and c of these rows: lane t loads row 32c + t; row 32c + e is then lane e's
+                // c of these rows: lane t loads row 32c + t; row 32c + e is then lane e's.  L comes
+                // from the copy in shared memory (one broadcast read)
                 const int it = i0 + 32 * c + lane;
-                const float Lt = it < a.Nq ? __ldg(lse_bh + it) * kLog2e : 0.f;
                 const float Ct = it < a.Nq ? __ldg(c_bh + it) : 0.f;
+                const float *Ls = reinterpret_cast<const float *>(smem + kOffL + (k & 1) * 512) + 32 * c;
                 uint32_t sv[32], dv[32];
                 ptx::tmem_ld32(lane_addr + 32 * c, sv);
                 ptx::tmem_ld32(lane_addr + 128 + 32 * c, dv);
@@ -284,20 +314,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t pp[16], dp[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float pe[2], de[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = i0 + 32 * c + e + u;
-                        const bool vis = j < n && i < a.Nq && (!a.causal || j <= i + shift);
-                        const float Li = __shfl_sync(0xffffffffu, Lt, e + u);
-                        const float Ci = __shfl_sync(0xffffffffu, Ct, e + u);
-                        const float p = vis ? ptx::ex2(__uint_as_float(sv[e + u]) * a.scale_log2 - Li) : 0.f;
-                        pe[u] = p;
-                        // a select, not a product: dP^T of a key past the sequence may be NaN
-                        de[u] = vis ? p * (__uint_as_float(dv[e + u]) - Ci) : 0.f;
-                    }
-                    pp[e / 2] = ptx::pack_bf16x2(pe[0], pe[1]);
-                    dp[e / 2] = ptx::pack_bf16x2(de[0], de[1]);
+                    const float2 L2 = *reinterpret_cast<const float2 *>(Ls + e);
+                    const float C0 = __shfl_sync(0xffffffffu, Ct, e), C1 = __shfl_sync(0xffffffffu, Ct, e + 1);
+                    float x0, x1, g0, g1;
+                    ptx::fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.scale_log2, a.scale_log2,
+                              -L2.x, -L2.y);
+                    ptx::add2(g0, g1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -C0, -C1);
+                    const int i = i0 + 32 * c + e;
+                    // visibility of rows i and i + 1 (selects, not products: anything stored past
+                    // the sequence, NaN included, is dropped)
+                    const bool v0 = j < n && i < a.Nq && (!a.causal || j <= i + shift);
+                    const bool v1 = j < n && i + 1 < a.Nq && (!a.causal || j <= i + 1 + shift);
+                    const float p0 = v0 ? ptx::ex2(x0) : 0.f, p1 = v1 ? ptx::ex2(x1) : 0.f;
+                    float d0, d1;
+                    ptx::mul2(d0, d1, p0, p1, g0, g1);
+                    pp[e / 2] = ptx::pack_bf16x2(p0, p1);
+                    dp[e / 2] = ptx::pack_bf16x2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
                 }
                 tmem_st16(lane_addr + 16 * c, pp);        // P^T over the S^T columns already read
                 tmem_st16(lane_addr + 128 + 16 * c, dp);  // dS^T over the dP^T columns already read
@@ -388,7 +420,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
-attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, cudaStream_t s) {
+attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, const float *lrow,
+                            cudaStream_t s) {
     const attn_fwd_params_t &f = p.fwd;
     CUtensorMap mq, mk, mv, mg;
     attn_status_t st;
@@ -400,7 +433,8 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     TcArgs a;
     a.B = (int)f.B; a.H = (int)f.H; a.Nq = (int)f.Nq; a.Nk = (int)f.Nk; a.causal = f.causal;
     a.scale = f.scale; a.scale_log2 = f.scale * kLog2e;
-    a.lse = f.lse; a.crow = crow; a.kv_lens = f.kv_lens; a.dq_acc = dq_acc;
+    a.crow = crow; a.lrow = lrow; a.nq_pad = (int)((f.Nq + 127) / 128 * 128);
+    a.kv_lens = f.kv_lens; a.dq_acc = dq_acc;
     a.dk = static_cast<__nv_bfloat16 *>(p.dk);
     a.dv = static_cast<__nv_bfloat16 *>(p.dv);
     a.dks0 = p.dk_stride[0]; a.dks1 = p.dk_stride[1]; a.dks2 = p.dk_stride[2];
