@@ -290,6 +290,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float *c_bh = a.crow + ((long long)b * a.H + h) * a.Nq;
         for (int k = 0; ok && k < ntiles; ++k) {
             const int i0 = (t_first + k) * BQ;
+            // c of the tile's rows, lane t holding rows 32c + t: loaded before the wait for S^T
+            float Cq[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int it = i0 + 32 * c + lane;
+                Cq[c] = it < a.Nq ? __ldg(c_bh + it) : 0.f;
+            }
             // s_full implies the tile's copies are done; waiting on their barrier as well makes
             // the copied L visible to these threads
             if (!wait_warp(&ctrl->s_full, k & 1) || !wait_warp(&ctrl->q_full[k & 1], (k >> 1) & 1) ||
@@ -300,10 +307,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ptx::tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {  // rows 32c .. 32c + 31 of the tile
-                // c of these rows: lane t loads row 32c + t; row 32c + e is then lane e's.  L comes
-                // from the copy in shared memory (one broadcast read)
-                const int it = i0 + 32 * c + lane;
-                const float Ct = it < a.Nq ? __ldg(c_bh + it) : 0.f;
+                // c of row 32c + e is lane e's Cq[c]; L comes from the copy in shared memory (one
+                // broadcast read)
+                const float Ct = Cq[c];
                 const float *Ls = reinterpret_cast<const float *>(smem + kOffL + (k & 1) * 512) + 32 * c;
                 uint32_t sv[32], dv[32];
                 ptx::tmem_ld32(lane_addr + 32 * c, sv);
@@ -390,22 +396,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ptx::tc_fence_after();
             const int i = (t_first + k) * BQ + r;
             float *dst = a.dq_acc + (((long long)b * a.Nq + i) * a.H + h) * 128;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t qv[32];
-                ptx::tmem_ld32(lane_addr + 128 + 32 * c, qv);
-                ptx::tmem_ld_wait();
-                ptx::reg_fence(qv);
-                if (i < a.Nq) {
+            // the whole row into registers first, so the columns are free for the next tile's
+            // dP^T before the reductions are issued
+            uint32_t qv[4][32];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        red_add_v4(dst + 32 * c + 4 * q, a.scale * __uint_as_float(qv[4 * q]),
-                                   a.scale * __uint_as_float(qv[4 * q + 1]), a.scale * __uint_as_float(qv[4 * q + 2]),
-                                   a.scale * __uint_as_float(qv[4 * q + 3]));
-                }
-            }
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(lane_addr + 128 + 32 * c, qv[c]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::reg_fence(qv[c]);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&ctrl->dq_free);
+            if (i < a.Nq) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        red_add_v4(dst + 32 * c + 4 * q, a.scale * __uint_as_float(qv[c][4 * q]),
+                                   a.scale * __uint_as_float(qv[c][4 * q + 1]),
+                                   a.scale * __uint_as_float(qv[c][4 * q + 2]),
+                                   a.scale * __uint_as_float(qv[c][4 * q + 3]));
+            }
         }
     }
 
