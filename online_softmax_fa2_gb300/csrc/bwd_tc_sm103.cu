@@ -8,20 +8,22 @@
 // of one (b, h) and walks the query tiles of 128 rows that see any of its keys:
 //
 //   TMEM (512 columns)   S^T / P^T [0, 128)   dP^T / dS^T [128, 256)   dV [256, 384)   dK [384, 512)
-//                        dQ of the tile goes into [128, 256) once dS^T has been read there, so
-//                        the next tile's S^T can start while dQ is read out.
+//                        dQ^T of the tile goes into [128, 256) once dS^T has been read there, so
+//                        the next tile's S^T can start while dQ^T is read out.
 //   S^T  = K Q^T         A = K, B = Q   (both [row][dim] in shared memory, K-major)
 //   dP^T = V G^T         A = V, B = G   (G: the upstream gradient dL/dO)
 //   P^T, dS^T            one thread per key (TMEM lane): mask, exp(x - L), (dP - c); P^T and
 //                        dS^T go back into TMEM as bf16, dS^T also into shared memory
 //   dV  += P^T G         A = P^T from TMEM, B = G read MN-major (as V in the forward's P V)
 //   dK  += dS^T Q        A = dS^T from TMEM, B = Q read MN-major
-//   dQ   = dS K          A = dS read MN-major from the [key][row] copy, B = K read MN-major
+//   dQ^T = K^T dS^T      A = K read MN-major, B = the [key][row] copy of dS^T read MN-major
+//                        (transposed so that a TMEM lane is one head dimension: a warp's
+//                        reduction of one row into dQ is then a single 128-byte line)
 //
 // Roles (384 threads): warp 0 loads K and V once and Q, G per tile with TMA; warp 1 issues the
 // products (one thread); warps 4-7 form P^T and dS^T and, at the end, write dK (times scale)
-// and dV; warps 8-11 read each tile's dQ from TMEM (one thread per row) and add scale * dQ to
-// the fp32 accumulator with vector reductions.  Every mbarrier wait is bounded as in the
+// and dV; warps 8-11 read each tile's dQ^T from TMEM (one thread per head dimension) and add
+// scale * dQ to the fp32 accumulator, one coalesced reduction per row and warp.  Every mbarrier wait is bounded as in the
 // forward kernels.
 #include "fwd_bf16_common.cuh"
 
@@ -97,9 +99,8 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, f
 }  // namespace ptx
 namespace {
 
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+__device__ __forceinline__ void red_add(float *addr, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_ab(BQ, BK, false, false);  // S^T, dP^T
             constexpr uint32_t kIdKV = idesc_ab(BQ, 128, false, true);  // dV, dK: A from TMEM, B MN-major
-            constexpr uint32_t kIdQ = idesc_ab(BQ, 128, true, true);    // dQ: A and B MN-major
+            constexpr uint32_t kIdQ = idesc_ab(128, BQ, true, true);    // dQ^T: A and B MN-major
             const uint32_t sK = ptx::smem_u32(smem + kOffK), sV = ptx::smem_u32(smem + kOffV);
             const uint32_t sS = ptx::smem_u32(smem + kOffS);
             bool ok = wait(&ctrl->kv_full, 0);
@@ -258,8 +259,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ptx::mma_ts(tmem + 384, tmem + 128 + kk * 8, qm + ((kk * 16 * 128) >> 4), kIdKV,
                                     (k > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // dQ = dS K into the columns dS^T occupied
-                        ptx::mma_ss(tmem + 128, sm_ + ((kk * 16 * 128) >> 4), km + ((kk * 16 * 128) >> 4), kIdQ,
+                    for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T into the columns dS^T occupied
+                        ptx::mma_ss(tmem + 128, km + ((kk * 16 * 128) >> 4), sm_ + ((kk * 16 * 128) >> 4), kIdQ,
                                     kk > 0 ? 1u : 0u);
                     ptx::mma_commit(&ctrl->dq_full);
                     ptx::mma_commit(&ctrl->ds_free);
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             return __all_sync(0xffffffffu, wait(bar, parity));
         };
         bool ok = wait_warp(&ctrl->kv_full, 0);
-        if (ok && j >= n) {  // K rows past the sequence may hold anything: zero them for dQ = dS K
+        if (ok && j >= n) {  // K rows past the sequence may hold anything: zero them for dQ^T = K^T dS^T
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 uint4 *dst = reinterpret_cast<uint4 *>(smem + kOffK + p * kPanelBytes + r * 128);
@@ -387,17 +388,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     } else if (warp >= 8) {
-        // ------------------------------------------------------------ dQ (one query row each)
-        const int r = (int)threadIdx.x - 256;
+        // ------------------------------------------------------------ dQ^T (one head dimension each)
+        const int d = (int)threadIdx.x - 256;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const long long row_stride = (long long)a.H * 128;
         for (int k = 0; k < ntiles; ++k) {
             const bool w = ptx::mbar_wait(&ctrl->dq_full, k & 1, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, w)) break;
             ptx::tc_fence_after();
-            const int i = (t_first + k) * BQ + r;
-            float *dst = a.dq_acc + (((long long)b * a.Nq + i) * a.H + h) * 128;
-            // the whole row into registers first, so the columns are free for the next tile's
-            // dP^T before the reductions are issued
+            const int i0 = (t_first + k) * BQ, rows = min(BQ, a.Nq - i0);
+            float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * 128 + d;
+            // the tile's 128 rows of this dimension into registers first, so the columns are free
+            // for the next tile's dP^T before the reductions are issued
             uint32_t qv[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(lane_addr + 128 + 32 * c, qv[c]);
@@ -406,16 +408,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < 4; ++c) ptx::reg_fence(qv[c]);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&ctrl->dq_free);
-            if (i < a.Nq) {
+            // row r of the tile: the warp's 32 lanes add 32 consecutive dimensions (one line)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        red_add_v4(dst + 32 * c + 4 * q, a.scale * __uint_as_float(qv[c][4 * q]),
-                                   a.scale * __uint_as_float(qv[c][4 * q + 1]),
-                                   a.scale * __uint_as_float(qv[c][4 * q + 2]),
-                                   a.scale * __uint_as_float(qv[c][4 * q + 3]));
-            }
+                for (int e = 0; e < 32; ++e)
+                    if (32 * c + e < rows) red_add(dst + (32 * c + e) * row_stride, a.scale * __uint_as_float(qv[c][e]));
         }
     }
 
