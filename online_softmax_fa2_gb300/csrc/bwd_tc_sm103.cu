@@ -8,8 +8,11 @@
 // of one (b, h) and walks the query tiles of 128 rows that see any of its keys:
 //
 //   TMEM (512 columns)   S^T / P^T [0, 128)   dP^T / dS^T [128, 256)   dV [256, 384)   dK [384, 512)
-//                        dQ^T of the tile goes into [128, 256) once dS^T has been read there, so
-//                        the next tile's S^T can start while dQ^T is read out.
+//                        Each tile is handled as two halves of 64 query rows with barriers of
+//                        their own (half h: S^T columns [64h, 64h + 64), dP^T [128 + 64h, ...)), so
+//                        that P^T and dS^T of one half are formed while the tensor cores run the
+//                        products of the other.  dQ^T of a half goes into that half's dP^T columns
+//                        once dK has read its dS^T there.
 //   S^T  = K Q^T         A = K, B = Q   (both [row][dim] in shared memory, K-major)
 //   dP^T = V G^T         A = V, B = G   (G: the upstream gradient dL/dO)
 //   P^T, dS^T            one thread per key (TMEM lane): mask, exp(x - L), (dP - c); P^T and
@@ -38,6 +41,7 @@ constexpr int kTile = 2 * kPanelBytes;  // 128 rows x 128 bf16: two 64-column 12
 constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffG = 4 * kTile, kOffS = 6 * kTile;
 constexpr int kOffL = 7 * kTile;         // lse * log2 e of the tile's 128 rows, two stages
 constexpr int kOffCtrl = kOffL + 2 * 512;
+constexpr int kHalf = BQ / 2;  // query rows of a half tile
 
 struct TcArgs {
     int B, H, Nq, Nk, causal;
@@ -53,7 +57,8 @@ struct TcArgs {
 };
 
 struct TcCtrl {
-    uint64_t kv_full, q_full[2], q_empty[2], s_full, p_ready, dq_full, dq_free, ds_free, kv_final;
+    // q_full, q_empty: per stage; s_full .. ds_free: per half tile
+    uint64_t kv_full, q_full[2], q_empty[2], s_full[2], p_ready[2], dq_full[2], dq_free[2], ds_free[2], kv_final;
     uint32_t tmem_base;
     int abort;
 };
@@ -145,11 +150,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ptx::mbar_init(&ctrl->q_full[st], 1);
             ptx::mbar_init(&ctrl->q_empty[st], 1);
         }
-        ptx::mbar_init(&ctrl->s_full, 1);
-        ptx::mbar_init(&ctrl->p_ready, 128);
-        ptx::mbar_init(&ctrl->dq_full, 1);
-        ptx::mbar_init(&ctrl->dq_free, 128);
-        ptx::mbar_init(&ctrl->ds_free, 1);
+        for (int hh = 0; hh < 2; ++hh) {
+            ptx::mbar_init(&ctrl->s_full[hh], 1);
+            ptx::mbar_init(&ctrl->p_ready[hh], 128);
+            ptx::mbar_init(&ctrl->dq_full[hh], 1);
+            ptx::mbar_init(&ctrl->dq_free[hh], 128);
+            ptx::mbar_init(&ctrl->ds_free[hh], 1);
+        }
         ptx::mbar_init(&ctrl->kv_final, 1);
         ctrl->abort = 0;
         ptx::fence_mbar_init();
@@ -211,61 +218,86 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ tensor-core issuer
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_ab(BQ, BK, false, false);  // S^T, dP^T
-            constexpr uint32_t kIdKV = idesc_ab(BQ, 128, false, true);  // dV, dK: A from TMEM, B MN-major
-            constexpr uint32_t kIdQ = idesc_ab(128, BQ, true, true);    // dQ^T: A and B MN-major
+            constexpr uint32_t kIdS = idesc_ab(BK, kHalf, false, false);  // S^T, dP^T of a half
+            constexpr uint32_t kIdKV = idesc_ab(BK, 128, false, true);    // dV, dK: A from TMEM, B MN-major
+            constexpr uint32_t kIdQ = idesc_ab(128, kHalf, true, true);   // dQ^T: A and B MN-major
             const uint32_t sK = ptx::smem_u32(smem + kOffK), sV = ptx::smem_u32(smem + kOffV);
             const uint32_t sS = ptx::smem_u32(smem + kOffS);
-            bool ok = wait(&ctrl->kv_full, 0);
+            // K-major operands: 16-dim steps are 32 bytes apart inside a 64-column panel
+            const uint64_t kd = ptx::sdesc_sw128(sK, 16, 1024), vd = ptx::sdesc_sw128(sV, 16, 1024);
+            // MN-major operands: 16-row steps are 16 rows x 128 bytes apart; the two 64-wide
+            // panels of the N (or M) dimension are kPanelBytes apart
+            const uint64_t km = ptx::sdesc_sw128(sK, kPanelBytes, 1024);
+            // S^T and dP^T of half hh of tile k (Q, G in stage k & 1); dP^T overwrites the
+            // previous tile's dQ^T of this half, so it waits until that has been read
+            auto s_dp = [&](int k, int hh) -> bool {
+                const uint32_t off_q = kOffQ + (k & 1) * kTile + hh * kHalf * 128;
+                const uint32_t off_g = kOffG + (k & 1) * kTile + hh * kHalf * 128;
+                const uint64_t qd = ptx::sdesc_sw128(ptx::smem_u32(smem + off_q), 16, 1024);
+                const uint64_t gd = ptx::sdesc_sw128(ptx::smem_u32(smem + off_g), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
+                    ptx::mma_ss(tmem + hh * kHalf, kd + off, qd + off, kIdS, kk > 0 ? 1u : 0u);
+                }
+                if (k > 0 && !wait(&ctrl->dq_free[hh], (k - 1) & 1)) return false;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
+                    ptx::mma_ss(tmem + 128 + hh * kHalf, vd + off, gd + off, kIdS, kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&ctrl->s_full[hh]);
+                return true;
+            };
+            // dV += P^T G, dK += dS^T Q over the half's 64 rows, then its dQ^T = K^T dS^T
+            auto grads = [&](int k, int hh) {
+                const uint32_t sQ = ptx::smem_u32(smem + kOffQ + (k & 1) * kTile);
+                const uint32_t sG = ptx::smem_u32(smem + kOffG + (k & 1) * kTile);
+                const uint64_t gm = ptx::sdesc_sw128(sG, kPanelBytes, 1024);
+                const uint64_t qm = ptx::sdesc_sw128(sQ, kPanelBytes, 1024);
+                const uint64_t sm_ = ptx::sdesc_sw128(sS + hh * kPanelBytes, kPanelBytes, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {  // P^T bf16 pairs: 8 columns per 16 rows
+                    const uint32_t row_off = ((hh * kHalf + kk * 16) * 128) >> 4;
+                    ptx::mma_ts(tmem + 256, tmem + hh * kHalf + kk * 8, gm + row_off, kIdKV,
+                                (k > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t row_off = ((hh * kHalf + kk * 16) * 128) >> 4;
+                    ptx::mma_ts(tmem + 384, tmem + 128 + hh * kHalf + kk * 8, qm + row_off, kIdKV,
+                                (k > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // into the columns the half's dS^T occupied
+                    ptx::mma_ss(tmem + 128 + hh * kHalf, km + ((kk * 16 * 128) >> 4), sm_ + ((kk * 16 * 128) >> 4),
+                                kIdQ, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&ctrl->dq_full[hh]);
+                ptx::mma_commit(&ctrl->ds_free[hh]);
+            };
+            bool ok = wait(&ctrl->kv_full, 0) && wait(&ctrl->q_full[0], 0);
+            if (ok) {
+                ptx::tc_fence_after();
+                ok = s_dp(0, 0) && s_dp(0, 1);
+            }
             for (int k = 0; ok && k < ntiles; ++k) {
-                const int st = k & 1;
-                const uint32_t sQ = ptx::smem_u32(smem + kOffQ + st * kTile), sG = ptx::smem_u32(smem + kOffG + st * kTile);
-                if (!wait(&ctrl->q_full[st], (k >> 1) & 1)) break;
+                const bool more = k + 1 < ntiles;
+                // half 0 of tile k, then S^T and dP^T of half 0 of tile k + 1 while the
+                // transform works on half 1
+                if (!wait(&ctrl->p_ready[0], k & 1)) break;
                 ptx::tc_fence_after();
-                {
-                    // K-major operands: 16-dim steps are 32 bytes apart inside a 64-column panel
-                    const uint64_t kd = ptx::sdesc_sw128(sK, 16, 1024), qd = ptx::sdesc_sw128(sQ, 16, 1024);
-                    const uint64_t vd = ptx::sdesc_sw128(sV, 16, 1024), gd = ptx::sdesc_sw128(sG, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
-                        ptx::mma_ss(tmem + 0, kd + off, qd + off, kIdS, kk > 0 ? 1u : 0u);
-                    }
-                    // dP^T goes where the previous tile's dQ was: wait until it has been read
-                    if (k > 0 && !wait(&ctrl->dq_free, (k - 1) & 1)) break;
+                grads(k, 0);
+                if (more) {
+                    if (!wait(&ctrl->q_full[(k + 1) & 1], ((k + 1) >> 1) & 1)) break;
                     ptx::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
-                        ptx::mma_ss(tmem + 128, vd + off, gd + off, kIdS, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(&ctrl->s_full);
+                    if (!s_dp(k + 1, 0)) break;
                 }
-                if (!wait(&ctrl->p_ready, k & 1)) break;
+                if (!wait(&ctrl->p_ready[1], k & 1)) break;
                 ptx::tc_fence_after();
-                {
-                    // MN-major operands: 16-row steps are 16 rows x 128 bytes apart; the two
-                    // 64-wide panels of the N (or M) dimension are kPanelBytes apart
-                    const uint64_t gm = ptx::sdesc_sw128(sG, kPanelBytes, 1024);
-                    const uint64_t qm = ptx::sdesc_sw128(sQ, kPanelBytes, 1024);
-                    const uint64_t km = ptx::sdesc_sw128(sK, kPanelBytes, 1024);
-                    const uint64_t sm_ = ptx::sdesc_sw128(sS, kPanelBytes, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // dV += P^T G: P^T bf16 pairs, 8 columns per 16 rows
-                        ptx::mma_ts(tmem + 256, tmem + 0 + kk * 8, gm + ((kk * 16 * 128) >> 4), kIdKV,
-                                    (k > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-                        ptx::mma_ts(tmem + 384, tmem + 128 + kk * 8, qm + ((kk * 16 * 128) >> 4), kIdKV,
-                                    (k > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T into the columns dS^T occupied
-                        ptx::mma_ss(tmem + 128, km + ((kk * 16 * 128) >> 4), sm_ + ((kk * 16 * 128) >> 4), kIdQ,
-                                    kk > 0 ? 1u : 0u);
-                    ptx::mma_commit(&ctrl->dq_full);
-                    ptx::mma_commit(&ctrl->ds_free);
-                    ptx::mma_commit(&ctrl->q_empty[st]);
-                }
+                grads(k, 1);
+                ptx::mma_commit(&ctrl->q_empty[k & 1]);  // the last reads of stage k & 1
+                if (more && !s_dp(k + 1, 1)) break;
             }
             ptx::mma_commit(&ctrl->kv_final);
             if (!ptx::mbar_wait_quiet(&ctrl->kv_final, 0, kWaitLimitNs)) atomicOr(a.flags, kFlagWaitTimeout);
@@ -298,16 +330,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int it = i0 + 32 * c + lane;
                 Cq[c] = it < a.Nq ? __ldg(c_bh + it) : 0.f;
             }
+            for (int hh = 0; ok && hh < 2; ++hh) {
             // s_full implies the tile's copies are done; waiting on their barrier as well makes
             // the copied L visible to these threads
-            if (!wait_warp(&ctrl->s_full, k & 1) || !wait_warp(&ctrl->q_full[k & 1], (k >> 1) & 1) ||
-                (k > 0 && !wait_warp(&ctrl->ds_free, (k - 1) & 1))) {
+            if (!wait_warp(&ctrl->s_full[hh], k & 1) || !wait_warp(&ctrl->q_full[k & 1], (k >> 1) & 1) ||
+                (k > 0 && !wait_warp(&ctrl->ds_free[hh], (k - 1) & 1))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {  // rows 32c .. 32c + 31 of the tile
+            for (int c = 2 * hh; c < 2 * hh + 2; ++c) {  // rows 32c .. 32c + 31 of the tile
                 // c of row 32c + e is lane e's Cq[c]; L comes from the copy in shared memory (one
                 // broadcast read)
                 const float Ct = Cq[c];
@@ -338,8 +371,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     pp[e / 2] = ptx::pack_bf16x2(p0, p1);
                     dp[e / 2] = ptx::pack_bf16x2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
                 }
-                tmem_st16(lane_addr + 16 * c, pp);        // P^T over the S^T columns already read
-                tmem_st16(lane_addr + 128 + 16 * c, dp);  // dS^T over the dP^T columns already read
+                // P^T and dS^T of the half packed into the first 32 of its S^T and dP^T columns
+                // (all read by now: chunk 2hh + 1 packs over chunk 2hh)
+                tmem_st16(lane_addr + 32 * hh + 16 * c, pp);
+                tmem_st16(lane_addr + 128 + 32 * hh + 16 * c, dp);
                 // dS^T into shared memory as [key][row]: rows 32c.. are 16-byte chunks
                 // 4 (c % 2) .. + 3 of panel c / 2, 128-byte swizzled like a TMA box
                 uint8_t *row = smem + kOffS + (c / 2) * kPanelBytes + r * 128;
@@ -353,7 +388,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ptx::tmem_st_wait();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&ctrl->p_ready);
+            ptx::mbar_arrive(&ctrl->p_ready[hh]);
+            }
         }
         // dK (times scale) and dV of this key
         if (ok && wait_warp(&ctrl->kv_final, 0)) {
@@ -392,28 +428,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int d = (int)threadIdx.x - 256;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const long long row_stride = (long long)a.H * 128;
-        for (int k = 0; k < ntiles; ++k) {
-            const bool w = ptx::mbar_wait(&ctrl->dq_full, k & 1, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
-            if (!__all_sync(0xffffffffu, w)) break;
-            ptx::tc_fence_after();
-            const int i0 = (t_first + k) * BQ, rows = min(BQ, a.Nq - i0);
-            float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * 128 + d;
-            // the tile's 128 rows of this dimension into registers first, so the columns are free
-            // for the next tile's dP^T before the reductions are issued
-            uint32_t qv[4][32];
+        bool ok = true;
+        for (int k = 0; ok && k < ntiles; ++k) {
+            for (int hh = 0; hh < 2; ++hh) {
+                const bool w = ptx::mbar_wait(&ctrl->dq_full[hh], k & 1, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int i0 = (t_first + k) * BQ + hh * kHalf, rows = min(kHalf, a.Nq - i0);
+                float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * 128 + d;
+                // the half's 64 rows of this dimension into registers first, so the columns are
+                // free for the next tile's dP^T before the reductions are issued
+                uint32_t qv[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(lane_addr + 128 + 32 * c, qv[c]);
-            ptx::tmem_ld_wait();
+                for (int c = 0; c < 2; ++c) ptx::tmem_ld32(lane_addr + 128 + hh * kHalf + 32 * c, qv[c]);
+                ptx::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::reg_fence(qv[c]);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&ctrl->dq_free);
-            // row r of the tile: the warp's 32 lanes add 32 consecutive dimensions (one line)
+                for (int c = 0; c < 2; ++c) ptx::reg_fence(qv[c]);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&ctrl->dq_free[hh]);
+                // row r of the half: the warp's 32 lanes add 32 consecutive dimensions (one line)
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (32 * c + e < rows) red_add(dst + (32 * c + e) * row_stride, a.scale * __uint_as_float(qv[c][e]));
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * c + e < rows)
+                            red_add(dst + (32 * c + e) * row_stride, a.scale * __uint_as_float(qv[c][e]));
+            }
         }
     }
 
