@@ -25,8 +25,9 @@
 //
 // Roles (384 threads): warp 0 loads K and V once and Q, G per tile with TMA; warp 1 issues the
 // products (one thread); warps 4-7 form P^T and dS^T and, at the end, write dK (times scale)
-// and dV; warps 8-11 read each tile's dQ^T from TMEM (one thread per head dimension) and add
-// scale * dQ to the fp32 accumulator, one coalesced reduction per row and warp.  Every mbarrier wait is bounded as in the
+// and dV; warps 8-11 read each tile's dQ^T from TMEM (one thread per head dimension), turn
+// blocks of 4 rows x 4 dimensions around among 4 lanes, and add scale * dQ to the fp32
+// accumulator with 16-byte reductions (a warp instruction covers 4 whole 128-byte rows).  Every mbarrier wait is bounded as in the
 // forward kernels.
 #include "fwd_bf16_common.cuh"
 
@@ -104,8 +105,28 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, f
 }  // namespace ptx
 namespace {
 
-__device__ __forceinline__ void red_add(float *addr, float v) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// 4 x 4 transpose among the lanes 4g .. 4g + 3 of a warp: on entry lane 4g + t holds x[s] =
+// M[s][t]; on exit it holds x[s] = M[t][s].  Two butterfly stages, each swapping the lane bit
+// with the index bit of the same weight (two shuffles per stage).
+__device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
+#pragma unroll
+    for (int bit = 1; bit <= 2; bit <<= 1) {
+        const bool hi = lane & bit;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            // the pair (lo, lo + bit) of indices that this stage exchanges
+            const int lo = bit == 1 ? 2 * j : j;
+            const float send = hi ? x[lo] : x[lo + bit];
+            const float got = __shfl_xor_sync(0xffffffffu, send, bit);
+            if (hi) x[lo] = got;
+            else x[lo + bit] = got;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -438,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const int i0 = (t_first + k) * BQ + hh * kHalf, rows = min(kHalf, a.Nq - i0);
-                float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * 128 + d;
+                float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * 128 + (d & ~3);
                 // the half's 64 rows of this dimension into registers first, so the columns are
                 // free for the next tile's dP^T before the reductions are issued
                 uint32_t qv[2][32];
@@ -449,13 +470,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int c = 0; c < 2; ++c) ptx::reg_fence(qv[c]);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&ctrl->dq_free[hh]);
-                // row r of the half: the warp's 32 lanes add 32 consecutive dimensions (one line)
+                // rows 4m .. 4m + 3 of the half: after the transpose lane 4g + s holds dimensions
+                // 4g .. 4g + 3 (of this warp's 32) of row 4m + s
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int m = 0; m < kHalf / 4; ++m) {
+                    float x[4];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * c + e < rows)
-                            red_add(dst + (32 * c + e) * row_stride, a.scale * __uint_as_float(qv[c][e]));
+                    for (int t = 0; t < 4; ++t) x[t] = a.scale * __uint_as_float(qv[m / 8][4 * (m % 8) + t]);
+                    transpose4(x, lane);
+                    const int row = 4 * m + (lane & 3);
+                    if (row < rows) red_add_v4(dst + row * row_stride, x[0], x[1], x[2], x[3]);
+                }
             }
         }
     }
