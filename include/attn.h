@@ -216,8 +216,9 @@ typedef struct {
 } attn_bwd_params_t;
 
 /*
- * Size in bytes of the workspace attn_bwd needs: an fp32 dQ accumulator [B, Nq, H, dk] and
- * the fp32 row terms c_i [B, H, Nq].  Returns 0 for a negative or zero size.
+ * Size in bytes of the workspace attn_bwd needs: an fp32 dQ accumulator [B, Nq, H, dk], the
+ * fp32 row terms c_i [B, H, Nq], and lse_i * log2 e [B, H, Nq rounded up to a multiple of 128]
+ * in fp32, each part starting on a 16-byte boundary.  Returns 0 for a negative or zero size.
  */
 size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk);
 
@@ -232,7 +233,9 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk);
  * The mask, bias, kv_lens and causal settings must be the forward's.  The bias is fixed: no
  * gradient is formed for it.  An empty row (lse = -inf) passes no gradient, and a key that no
  * row sees gets dK = dV = 0.
- * Queues three kernels on `stream`.  Supported: bfloat16, dk == dv in {64, 128}; every tensor
+ * Queues three kernels on `stream`: the row terms, the products (on the 5th-generation
+ * tensor cores for dk = dv = 128 without a bias, on warp-level tensor-core tiles otherwise),
+ * and the conversion of dQ to bf16.  Supported: bfloat16, dk == dv in {64, 128}; every tensor
  * 16-byte aligned with strides that are multiples of 8 elements.  The workspace is
  * caller-owned device memory of at least attn_bwd_workspace_bytes(B, H, Nq, dk) bytes,
  * 16-byte aligned; its contents on entry do not matter.  dQ is accumulated with atomic
