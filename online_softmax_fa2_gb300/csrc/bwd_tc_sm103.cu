@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcCtrl *ctrl = reinterpret_cast<TcCtrl *>(smem + kOffCtrl);
     volatile int *abort = &ctrl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // key block slowest: CTAs are dispatched in order of their linear index, so with a causal
+    // mask (block kb sees the query tiles from about kb on) the longest blocks of every head
+    // start first and the short ones fill the tail
+    const int h = blockIdx.x, b = blockIdx.y, kb = blockIdx.z;
 
     int n = a.Nk;
     if (a.kv_lens) {
@@ -519,7 +522,9 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    dim3 grid((unsigned)((f.Nk + BK - 1) / BK), (unsigned)f.H, (unsigned)f.B);
+    if ((f.Nk + BK - 1) / BK > 65535 || f.B > 65535)
+        return fail(ATTN_ERR_UNSUPPORTED, "backward supports B <= 65535 and Nk <= %d", 65535 * BK);
+    dim3 grid((unsigned)f.H, (unsigned)f.B, (unsigned)((f.Nk + BK - 1) / BK));
     bwd_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(mq, mk, mv, mg, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward (tcgen05) launch: %s", cudaGetErrorString(e));
