@@ -377,6 +377,50 @@ def run_ours(args):
                                                         ("decode.cu",))}}
         del d, ws
 
+    # backward of the same workload (dQ, dK, dV from o, lse and a seeded random dO): reported
+    # beside the forward's line with its own tensor roofline, taken over the whole backward
+    # step (row terms, products, dQ conversion: three launches)
+    bwd = None
+    if not args.no_backward:
+        o_b, l_b = ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        dout_b = torch.randn(o_b.shape, generator=gen, device=dev).to(o_b.dtype)
+        ws_b = torch.empty(ofa.bwd_workspace_bytes(a.B, a.H, a.Nq, a.dk) // 4 + 4, dtype=torch.float32,
+                           device=dev)
+        gq, gk, gv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
+
+        def bstep():
+            ofa.attn_bwd(a.q, a.k, a.v, o_b, l_b, dout_b, causal=True, scale=a.scale, dq=gq, dk=gk, dv=gv,
+                         workspace=ws_b)
+
+        for _ in range(max(3, min(args.warmup, 10))):
+            flush.zero_()
+            bstep()
+        nb = max(5, min(args.steps, 50))
+        evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
+        barrier()
+        for s_, e_ in evb:
+            flush.zero_()            # L2 flush, outside the timed interval
+            s_.record(stream)
+            bstep()
+            e_.record(stream)
+        barrier()
+        if ofa.device_error_flags() & 1:
+            raise RuntimeError("a backward kernel gave up a bounded wait during the timed region")
+        ms_b = max_over_ranks(sum(s_.elapsed_time(e_) for s_, e_ in evb) / nb, world, dev)
+        bflops = a.visible_pairs() * (6 * a.dk + 4 * a.dv)   # five products per visible pair
+        tb = job_rate(1, bflops, ms_b)
+        bwd = {"workload": "bf16_causal_b4_h16_n2048_d128_backward", "value": job_rate(world, bflops, ms_b),
+               "unit": "TFLOP/s", "ms_per_step": ms_b, "steps": nb, "flops_per_step": bflops,
+               "gpu_launches_per_step": 3, "l2": "flushed before every step",
+               "roofline": {"bound": "tensor", "achieved": tb, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": tb / pk["bf16_tflops"], "peak_kind": f"{pk_kind} dense bf16 (burst)",
+                            "frac_nominal": tb / NOMINAL["bf16_tflops"],
+                            "over": "the whole backward step (bwd_prep_kernel, bwd_tc_kernel, bwd_dq_kernel)",
+                            "traffic": None}}
+        del o_b, l_b, dout_b, ws_b, gq, gk, gv
+
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -402,6 +446,8 @@ def run_ours(args):
     }
     if dec:
         line["decode"] = dec
+    if bwd is not None:
+        line["backward"] = bwd
     if rank == 0 and not args.no_cpu:
         val, secs, sample, threads, nheads = cpu_oracle_sample(a, args.cpu_seconds)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
@@ -498,6 +544,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--case", choices=sorted(CASES), default=None,
