@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
+#include "sm100_ptx.cuh"
 #include "warp_mma.cuh"
 
 namespace attn {
@@ -84,6 +85,7 @@ __device__ __forceinline__ int seq_n(const BwdArgs &a, int b, bool report) {
 // each with 16-byte loads of o and g
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
+    ptx::launch_dependents();  // the products kernel may start its own loads meanwhile
     constexpr int LPR = D / 8;  // lanes per row
     const int rows = a.B * a.Nq * a.H;
     const int row = (blockIdx.x * 256 + threadIdx.x) / LPR, sub = threadIdx.x % LPR;
@@ -345,6 +347,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_main_kernel(BwdArgs a) {
 // thread (two 16-byte loads, one 16-byte store)
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(BwdArgs a) {
+    ptx::grid_dep_wait();  // the accumulator is complete once the products kernel is
     const int rows = a.B * a.Nq * a.H;
     const int x = blockIdx.x * 256 + threadIdx.x, row = x / (D / 8), c = 8 * (x % (D / 8));
     if (row >= rows) return;
@@ -386,8 +389,18 @@ cudaError_t launch_all(const BwdArgs &a, const attn_bwd_params_t &p, cudaStream_
         }
     }
     if (rows > 0) {
-        bwd_dq_kernel<D><<<row_blocks, 256, 0, st>>>(a);
-        return cudaGetLastError();
+        // launched with programmatic stream serialization: its CTAs may be scheduled while the
+        // products kernel drains, and wait there for it to complete
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(row_blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D>, a);
     }
     return cudaSuccess;
 }

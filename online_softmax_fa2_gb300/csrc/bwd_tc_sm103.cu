@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool any = j0 < n && i_first < a.Nq;
     const int t_first = i_first / BQ, t_end = any ? (a.Nq + BQ - 1) / BQ : t_first;
 
+    // the dQ conversion queued after this kernel may be scheduled (it waits for completion)
+    ptx::launch_dependents();
     if (!any) {  // no row sees a key of this block: dK = dV = 0
         if (warp >= 4 && warp < 8) {
             const int j = j0 + (int)threadIdx.x - 128;
@@ -194,11 +196,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ptx::tma_load_4d(smem + kOffV + p * kPanelBytes, &tm_v, &ctrl->kv_full, p * 64, j0, h, b);
         }
         ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], 2 * kTile + 512);
-        bulk_load(smem + kOffL, a.lrow + ((long long)b * a.H + h) * a.nq_pad + t_first * BQ, 512, &ctrl->q_full[0]);
         for (int p = 0; p < 2; ++p) {
             ptx::tma_load_4d(smem + kOffQ + p * kPanelBytes, &tm_q, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
             ptx::tma_load_4d(smem + kOffG + p * kPanelBytes, &tm_g, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
         }
+        // lse * log2 e, the row terms c and the zeroed dQ accumulator come from the prep kernel,
+        // which this launch may overlap: every role that touches them waits for it first
+        ptx::grid_dep_wait();
+        bulk_load(smem + kOffL, a.lrow + ((long long)b * a.H + h) * a.nq_pad + t_first * BQ, 512, &ctrl->q_full[0]);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&ctrl->tmem_base, 512);
@@ -344,6 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         ptx::fence_proxy_async_smem();
+        ptx::grid_dep_wait();
         const float *c_bh = a.crow + ((long long)b * a.H + h) * a.Nq;
         for (int k = 0; ok && k < ntiles; ++k) {
             const int i0 = (t_first + k) * BQ;
@@ -452,6 +458,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int d = (int)threadIdx.x - 256;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const long long row_stride = (long long)a.H * 128;
+        ptx::grid_dep_wait();
         bool ok = true;
         for (int k = 0; ok && k < ntiles; ++k) {
             for (int hh = 0; hh < 2; ++hh) {
@@ -524,9 +531,19 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     if ((f.Nk + BK - 1) / BK > 65535 || f.B > 65535)
         return fail(ATTN_ERR_UNSUPPORTED, "backward supports B <= 65535 and Nk <= %d", 65535 * BK);
-    dim3 grid((unsigned)f.H, (unsigned)f.B, (unsigned)((f.Nk + BK - 1) / BK));
-    bwd_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(mq, mk, mv, mg, a);
-    e = cudaGetLastError();
+    // programmatic stream serialization: CTAs may start (TMEM, barriers, the K, V, Q, dO
+    // copies) while the prep kernel drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)f.H, (unsigned)f.B, (unsigned)((f.Nk + BK - 1) / BK));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel, mq, mk, mv, mg, a);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward (tcgen05) launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }

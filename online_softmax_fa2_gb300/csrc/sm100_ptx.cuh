@@ -87,6 +87,13 @@ __device__ __forceinline__ bool mbar_wait_quiet(uint64_t *bar, uint32_t parity, 
 
 // ------------------------------------------------------------------ TMA
 
+// Programmatic dependent launch.  launch_dependents: this CTA no longer holds back the launch
+// of a grid queued after it with programmatic stream serialization.  grid_dep_wait: blocks
+// until the grids this one depends on have completed and their memory is visible (a no-op
+// when the grid was launched without that attribute).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
