@@ -216,3 +216,21 @@ STANDARD = {
     "bf16_causal_b1_h32_n16384_d128": long_causal,
     "bf16_decode_b64_h32_l8192_d128": decode,
 }
+
+
+def dropout_keep(B, H, Nq, Nk, p_drop, seed=0, device="cpu"):
+    """Seeded keep mask [B, H, Nq, Nk] (bool): each position kept with probability 1 - p_drop."""
+    g = _gen("cpu", seed + 2000)
+    keep = torch.rand((B, H, Nq, Nk), generator=g) >= p_drop
+    return keep.to(device)
+
+
+def pack_keep_mask(keep):
+    """Bit-packed keep mask for attn_fwd: uint8 [B, H, Nq, 16 * ceil(Nk / 128)], bit (j % 8) of
+    byte j // 8 of a row = key j kept (rows padded with zero bytes to whole 128-key tiles)."""
+    B, H, Nq, Nk = keep.shape
+    nb = 16 * ((Nk + 127) // 128)
+    bits = torch.zeros((B, H, Nq, nb * 8), dtype=torch.uint8, device=keep.device)
+    bits[..., :Nk] = keep.to(torch.uint8)
+    weights = torch.tensor([1, 2, 4, 8, 16, 32, 64, 128], dtype=torch.uint8, device=keep.device)
+    return (bits.view(B, H, Nq, nb, 8) * weights).sum(-1).to(torch.uint8)

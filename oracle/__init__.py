@@ -177,6 +177,36 @@ def attn_probs(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, lib=N
     return p
 
 
+def attn_fwd_dropout(q, k, v, keep, p_drop, bias=None, kv_lens=None, causal=False, scale=None,
+                     lib=None):
+    """Attention with dropout on the normalised weights, in float64 (small inputs only).
+
+    "How Does FlashAttention Preserve Global Softmax Across Tiles?", section 6, disables
+    dropout and adds that with training dropout the backward recomputation must reproduce the
+    forward's random mask and scaling.  The reading taken here is inverted dropout of the
+    weights: keep [B, H, Nq, Nk] (nonzero = kept) is an input, so forward and backward see
+    the same mask; O_i = sum_j keep_ij / (1 - p_drop) * P_ij v_j with P the weights of
+    attn_probs (the row's undropped softmax); lse is the undropped log-sum-exp of attn_fwd.
+    Returns (O float64 [B, Nq, H, dv], lse float64 [B, H, Nq])."""
+    if not 0.0 <= p_drop < 1.0:
+        raise ValueError("p_drop must be in [0, 1)")
+    P = attn_probs(q, k, v, bias=bias, kv_lens=kv_lens, causal=causal, scale=scale, lib=lib)
+    keep = np.asarray(keep.cpu().numpy() if hasattr(keep, "cpu") else keep) != 0
+    if keep.shape != P.shape:
+        raise ValueError(f"keep shape {keep.shape}, expected {P.shape}")
+    w = np.where(keep, P, 0.0) / (1.0 - p_drop)
+    # the sum runs over visible keys only: value rows past a sequence's key length are no
+    # part of it (they may hold anything), so they are left out, not multiplied by zero
+    v64 = _f32(v).astype(np.float64)
+    kvl = _kvl(kv_lens)
+    if kvl is not None:
+        for b in range(v64.shape[0]):
+            v64[b, min(max(int(kvl[b]), 0), v64.shape[1]):] = 0.0
+    o = np.einsum("bhij,bjhd->bihd", w, v64)
+    _, lse, _ = attn_fwd(q, k, v, bias=bias, kv_lens=kv_lens, causal=causal, scale=scale, lib=lib)
+    return o, lse
+
+
 def key_state(q, k, v, j0, j1, bias=None, kv_lens=None, causal=False, scale=None,
               lib=None):
     """State (m, l, u) of every row over the visible keys in [j0, j1): [B, H, Nq, 2 + dv]."""
