@@ -464,6 +464,7 @@ def run_ours(args):
 CASES = {
     # name: (workload factory kwargs, kind)
     "prefill": ("causal_2k", {}, "fwd"),
+    "prefill_dropout": ("causal_2k", {}, "fwd_dropout"),
     "padbias": ("padded_bias", {}, "fwd"),
     "long_causal": ("long_causal", {}, "fwd"),
     "fp32": ("fp32_small", {}, "fwd"),
@@ -488,11 +489,15 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     a = getattr(wl, fac)(dev, **kw)
     ofa.load()
-    if kind == "fwd":
+    if kind in ("fwd", "fwd_dropout"):
         o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
         lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
+        mask, p_drop = None, 0.0
+        if kind == "fwd_dropout":  # a seeded keep mask with p = 0.1, bit-packed (33.5 MB here)
+            p_drop = 0.1
+            mask = wl.pack_keep_mask(wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p_drop, seed=1, device=dev))
         fn = lambda: ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
-                                  scale=a.scale, out=o, lse=lse)
+                                  scale=a.scale, out=o, lse=lse, dropout_mask=mask, dropout_p=p_drop)
         work, unit = a.flops() / 1e12, "TFLOP/s"
     elif kind == "bwd":
         o, lse = ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,

@@ -95,6 +95,20 @@ typedef enum {
  *   multiples of 8 elements (16 bytes); bias 4-byte aligned (rows that are 16-byte aligned
  *   are read with 16-byte loads).
  * float32 path (exact fp32 SIMT): 1 <= dk, dv <= 256; any finite scale.
+ *
+ *   dropout_mask        NULL: no dropout.  Otherwise the keep mask of a training forward:
+ *                       key j of row i of (b, h) is kept iff bit (j % 8) of byte
+ *                       dropout_mask[b*s0 + h*s1 + i*s2 + j/8] is set (s = dropout_mask_stride,
+ *                       in bytes; each row holds at least 16*ceil(Nk/128) bytes).  Kept
+ *                       weights p_ij are scaled by 1 / (1 - dropout_p), dropped ones count 0
+ *                       in o; the row sum and lse are those of the undropped softmax.  The
+ *                       mask is an input so that a backward can reproduce it ("How Does
+ *                       FlashAttention Preserve Global Softmax Across Tiles?", section 6,
+ *                       disables dropout and asks exactly that of a training backward).
+ *                       bfloat16: dk <= 128 only, the mask 16-byte aligned with strides that
+ *                       are multiples of 16 bytes.  Not taken by attn_decode_splitkv or
+ *                       attn_bwd (ATTN_ERR_UNSUPPORTED).
+ *   dropout_p           in [0, 1) with a mask; must be 0 without one.
  */
 typedef struct {
     int32_t dtype;           /* attn_dtype_t */
@@ -114,6 +128,9 @@ typedef struct {
     const int32_t *kv_lens;
     float scale;
     int32_t block_k;
+    const uint8_t *dropout_mask;
+    int64_t dropout_mask_stride[3];  /* b, h, i (bytes) */
+    float dropout_p;
 } attn_fwd_params_t;
 
 /*

@@ -66,6 +66,8 @@ class Params(ctypes.Structure):
         ("bias_stride", ctypes.c_int64 * 3),
         ("kv_lens", ctypes.c_void_p),
         ("scale", ctypes.c_float), ("block_k", ctypes.c_int32),
+        ("dropout_mask", ctypes.c_void_p), ("dropout_mask_stride", ctypes.c_int64 * 3),
+        ("dropout_p", ctypes.c_float),
     ]
 
 
@@ -164,9 +166,9 @@ def _require_cuda(*ts):
 
 
 def make_params(q, k, v, o, lse=None, bias=None, kv_lens=None, causal=False, scale=None,
-                block_k=0) -> Params:
+                block_k=0, dropout_mask=None, dropout_p=0.0) -> Params:
     """Fill an attn_fwd_params_t from tensors (no computation)."""
-    _require_cuda(q, k, v, o, lse, bias, kv_lens)
+    _require_cuda(q, k, v, o, lse, bias, kv_lens, dropout_mask)
     B, Nq, H, dk = q.shape
     Nk, dv = k.shape[1], v.shape[3]
     if k.shape != (B, Nk, H, dk) or v.shape != (B, Nk, H, dv) or o.shape != (B, Nq, H, dv):
@@ -201,12 +203,26 @@ def make_params(q, k, v, o, lse=None, bias=None, kv_lens=None, causal=False, sca
         p.kv_lens = kv_lens.data_ptr()
     p.scale = float(1.0 / math.sqrt(dk) if scale is None else scale)
     p.block_k = int(block_k)
+    if dropout_mask is not None:
+        nb = 16 * ((Nk + 127) // 128)
+        if dropout_mask.dtype != torch.uint8 or dropout_mask.dim() != 4 or dropout_mask.shape[3] < nb:
+            raise ValueError(f"dropout_mask must be uint8 [B, H, Nq, >= {nb}] (bit j % 8 of byte j // 8 "
+                             "keeps key j; see workloads.pack_keep_mask)")
+        mm = dropout_mask.expand(B, H, Nq, dropout_mask.shape[3])
+        if mm.stride(3) != 1:
+            raise ValueError("dropout_mask: the byte dimension must be contiguous")
+        p.dropout_mask = mm.data_ptr()
+        p.dropout_mask_stride = (ctypes.c_int64 * 3)(mm.stride(0), mm.stride(1), mm.stride(2))
+    p.dropout_p = float(dropout_p)
     return p
 
 
 def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, block_k=0, out=None,
-             lse=None, stream=None):
-    """Exact attention forward; returns (o, lse).  See include/attn.h, attn_fwd."""
+             lse=None, stream=None, dropout_mask=None, dropout_p=0.0):
+    """Exact attention forward; returns (o, lse).  See include/attn.h, attn_fwd.  With a
+    dropout_mask (uint8 [B, H, Nq, 16 * ceil(Nk / 128)], workloads.pack_keep_mask) the kept
+    weights are scaled by 1 / (1 - dropout_p) and the dropped ones count 0 in o; lse is the
+    undropped one."""
     lib = load()
     B, Nq, H, _ = q.shape
     dv = v.shape[3]
@@ -214,7 +230,7 @@ def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, block_k
         out = torch.empty((B, Nq, H, dv), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, block_k)
+    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, block_k, dropout_mask, dropout_p)
     _check(lib.attn_fwd(ctypes.byref(p), _stream(stream)))
     return out, lse
 

@@ -89,6 +89,13 @@ static attn_status_t check_common(const attn_fwd_params_t *p) {
         for (int i = 0; i < 3; ++i)
             if (p->bias_stride[i] < 0)
                 return fail(ATTN_ERR_INVALID_ARG, "bias_stride[%d] is negative", i);
+    if (p->dropout_mask) {
+        if (!(p->dropout_p >= 0.0f && p->dropout_p < 1.0f))
+            return fail(ATTN_ERR_INVALID_ARG, "dropout_p must be in [0, 1) (got %g)", p->dropout_p);
+        if ((st = check_strides("dropout_mask", p->dropout_mask_stride))) return st;
+    } else if (p->dropout_p != 0.0f) {
+        return fail(ATTN_ERR_INVALID_ARG, "dropout_p = %g without a dropout_mask", p->dropout_p);
+    }
     if (p->B * p->H * p->Nq == 0) return ATTN_OK;
     if (!p->q || !p->o) return fail(ATTN_ERR_INVALID_ARG, "q or o is NULL");
     if (p->Nk > 0 && (!p->k || !p->v))
@@ -137,6 +144,11 @@ extern "C" attn_status_t attn_fwd(const attn_fwd_params_t *p, attn_stream_t stre
         return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
     if (p->bias && (reinterpret_cast<uintptr_t>(p->bias) & 3u))
         return fail(ATTN_ERR_MISALIGNED, "bias must be 4-byte aligned");
+    if (p->dropout_mask) {
+        if (p->dk > 128) return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 dropout supports dk <= 128");
+        if (!aligned16(p->dropout_mask) || !stride_mult(p->dropout_mask_stride, 16))
+            return fail(ATTN_ERR_MISALIGNED, "dropout_mask must be 16-byte aligned with strides that are multiples of 16 bytes");
+    }
     return launch_fwd_bf16(*p, s);
 }
 
@@ -163,6 +175,7 @@ extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t
         return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [1, 256] (got %d)", num_splits);
     if (p->dtype != ATTN_DTYPE_BF16)
         return fail(ATTN_ERR_UNSUPPORTED, "decode supports bfloat16 only");
+    if (p->dropout_mask) return fail(ATTN_ERR_UNSUPPORTED, "decode takes no dropout mask");
     if (p->dk != p->dv || (p->dk != 64 && p->dk != 128))
         return fail(ATTN_ERR_UNSUPPORTED, "decode supports dk == dv in {64, 128} (dk=%lld dv=%lld)",
                     (long long)p->dk, (long long)p->dv);
@@ -228,6 +241,7 @@ extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, s
     attn_status_t st = check_common(f);
     if (st) return st;
     if (f->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward supports bfloat16 only");
+    if (f->dropout_mask) return fail(ATTN_ERR_UNSUPPORTED, "the backward of a dropout forward is not built");
     if (f->dk != f->dv || (f->dk != 64 && f->dk != 128))
         return fail(ATTN_ERR_UNSUPPORTED, "backward supports dk == dv in {64, 128} (dk=%lld dv=%lld)",
                     (long long)f->dk, (long long)f->dv);

@@ -38,6 +38,14 @@ struct Args {
     uint32_t *flags;
 };
 
+// Dropout of a training forward: keep bits (bit j % 8 of byte j / 8 of a row), or null.  A
+// kernel argument of its own, so that the kernels without dropout keep their argument block.
+struct DropArgs {
+    const uint8_t *dmask;
+    long long dms0, dms1, dms2;
+    float inv_keep;  // 1 / (1 - dropout_p)
+};
+
 // Key length of sequence b, clamped to [0, Nk] (a clamp is reported once per sequence).
 __device__ __forceinline__ int seq_len(const Args &a, int b, bool report) {
     if (!a.kv_lens) return a.Nk;
@@ -305,7 +313,7 @@ __device__ __forceinline__ void zero_v_row(uint8_t *sV, int row) {
 // Launches the two-tile kernel (dk <= 128); defined in fwd_bf16_pair_sm103.cu.
 attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
                                    const CUtensorMap &mv, const CUtensorMap &mo,
-                                   const bf16fwd::Args &a, int dk, int dv, bool bias,
+                                   const bf16fwd::Args &a, const bf16fwd::DropArgs &dr, int dk, int dv, bool bias,
                                    cudaStream_t s);
 
 }  // namespace attn

@@ -108,12 +108,25 @@ __device__ __forceinline__ Item next_item(const Args &a, int r, int c, int G, in
     return none;
 }
 
-template <int DK, int DV, bool kBias>
+// Dropout (training forward): the 128 keep bits of a row for one key tile, as four 32-bit
+// words (bit t of word w = key 32w + t of the tile), applied to p after the row sum has taken
+// it: kept weights scaled by 1 / (1 - dropout_p), dropped ones 0.
+__device__ __forceinline__ void apply_keep(float (&x)[BK], const uint4 &keep, float inv_keep) {
+    const uint32_t w[4] = {keep.x, keep.y, keep.z, keep.w};
+#pragma unroll
+    for (int k = 0; k < BK; ++k) x[k] = ((w[k >> 5] >> (k & 31)) & 1u) ? x[k] * inv_keep : 0.f;
+}
+
+__device__ __forceinline__ uint4 ld_keep(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+template <int DK, int DV, bool kBias, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_o, const Args a) {
+                         const __grid_constant__ CUtensorMap tm_o, const Args a, const DropArgs dr) {
     using L = Layout<DK, DV>;
     constexpr int KS = L::kKStages, VS = L::kVStages;
     constexpr bool kStageA = DV <= DK;  // tile A's output fits in its Q buffer
@@ -385,6 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_run = -INFINITY, l_run = 0.f;
             float x[BK];  // with a bias: the next tile's bias, loaded ahead
             if (kBias) load_bias(bias_row, bias_vec, 0, it.n, x);
+            // dropout: this row's keep bits, 16 bytes per key tile, the next tile's loaded ahead
+            const uint8_t *keep_row = nullptr;
+            uint4 keep = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (kDrop) {
+                if (i < a.Nq) {
+                    keep_row = dr.dmask + it.b * dr.dms0 + it.h * dr.dms1 + (long long)i * dr.dms2;
+                    keep = ld_keep(keep_row);
+                }
+            }
             for (int j = 0; j < nX; ++j) {
                 const int kv0 = j * BK, gj = g + j;
                 if (!wait_warp(&ctrl->s_full[X], (u + j) & 1)) {
@@ -400,6 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = update_max(mt, m_run, rescale);
                 const float lsum = tile_exp<kBias>(x, c, m_run);
                 l_run = fmaf(alpha, l_run, lsum);
+                if constexpr (kDrop) {  // the row sum keeps the undropped weights
+                    apply_keep(x, keep, dr.inv_keep);
+                    if (keep_row && j + 1 < nX) keep = ld_keep(keep_row + (j + 1) * (BK / 8));
+                }
                 if (__any_sync(0xffffffffu, rescale)) scale_o<DV>(lane_addr + o_col, alpha);
                 // value rows past n inside this tile may hold anything: the warpgroup of the
                 // first query tile that uses V_j zeroes them before its product reads V_j
@@ -465,11 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int DK, int DV, bool kBias>
+template <int DK, int DV, bool kBias, bool kDrop>
 attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                       const CUtensorMap &mo, const Args &a, cudaStream_t s) {
+                       const CUtensorMap &mo, const Args &a, const DropArgs &dr, cudaStream_t s) {
     const int smem = Layout<DK, DV>::kBytes;
-    auto kern = fwd_bf16_pair_kernel<DK, DV, kBias>;
+    auto kern = fwd_bf16_pair_kernel<DK, DV, kBias, kDrop>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const long long total = (long long)a.n_items * a.B * a.H;
@@ -478,7 +504,7 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     const int sms = sm_count();
     if (sms <= 0) return fail(ATTN_ERR_CUDA, "could not read the SM count");
     const unsigned grid = (unsigned)(total < sms ? total : sms);
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, a);
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, a, dr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16_pair launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
@@ -488,12 +514,16 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 
 attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
                                    const CUtensorMap &mv, const CUtensorMap &mo,
-                                   const bf16fwd::Args &a, int dk, int dv, bool bias,
+                                   const bf16fwd::Args &a, const bf16fwd::DropArgs &dr, int dk, int dv, bool bias,
                                    cudaStream_t s) {
 #define ATTN_PAIR_CASE(DK_, DV_)                                                              \
-    if (dk == DK_ && dv == DV_)                                                                \
-        return bias ? launch_t<DK_, DV_, true>(mq, mk, mv, mo, a, s)                           \
-                    : launch_t<DK_, DV_, false>(mq, mk, mv, mo, a, s);
+    if (dk == DK_ && dv == DV_) {                                                              \
+        if (dr.dmask)                                                                          \
+            return bias ? launch_t<DK_, DV_, true, true>(mq, mk, mv, mo, a, dr, s)                 \
+                        : launch_t<DK_, DV_, false, true>(mq, mk, mv, mo, a, dr, s);               \
+        return bias ? launch_t<DK_, DV_, true, false>(mq, mk, mv, mo, a, dr, s)                    \
+                    : launch_t<DK_, DV_, false, false>(mq, mk, mv, mo, a, dr, s);                  \
+    }
     ATTN_PAIR_CASE(128, 128)
     ATTN_PAIR_CASE(64, 64)
     ATTN_PAIR_CASE(128, 64)

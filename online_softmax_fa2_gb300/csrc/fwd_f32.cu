@@ -35,6 +35,9 @@ struct F32Args {
     long long bs0, bs1, bs2;
     const int *kv_lens;
     uint32_t *flags;
+    const uint8_t *dmask;  // dropout keep bits (bit j % 8 of byte j / 8 of a row), or null
+    long long dms0, dms1, dms2;
+    float inv_keep;        // 1 / (1 - dropout_p)
 };
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -145,7 +148,12 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(F32Args a) {
             for (int u = 0; u < (BK + 31) / 32; ++u) {
                 const int jj = lane + 32 * u;
                 float p = vis[u] ? expf(x[u] - m_new) : 0.f;
-                psum += p;
+                psum += p;  // the row sum keeps the undropped weight
+                if (a.dmask && vis[u]) {  // dropout: kept weights scaled, dropped ones 0 in o
+                    const int j = j0 + jj;
+                    const uint8_t bits = a.dmask[b * a.dms0 + h * a.dms1 + (long long)i * a.dms2 + (j >> 3)];
+                    p = ((bits >> (j & 7)) & 1u) ? p * a.inv_keep : 0.f;
+                }
                 if (jj < BK) Ps[warp * BK + jj] = p;
             }
             psum = warp_sum(psum);
@@ -211,6 +219,9 @@ attn_status_t launch_fwd_f32(const attn_fwd_params_t &p, cudaStream_t s) {
     a.bias = p.bias;
     a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1]; a.bs2 = p.bias_stride[2];
     a.kv_lens = p.kv_lens;
+    a.dmask = p.dropout_mask;
+    a.dms0 = p.dropout_mask_stride[0]; a.dms1 = p.dropout_mask_stride[1]; a.dms2 = p.dropout_mask_stride[2];
+    a.inv_keep = p.dropout_mask ? (float)(1.0 / (1.0 - (double)p.dropout_p)) : 1.f;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     if (p.B > 65535 || p.H > 65535)

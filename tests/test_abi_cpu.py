@@ -150,3 +150,40 @@ def test_bwd_rejects_bad_arguments_on_the_host(lib):
     p.dq = 0x80004  # not 16-byte aligned
     assert lib.attn_bwd(ctypes.byref(p), ws, need, None) == ofa.Status.MISALIGNED
     assert lib.attn_bwd_workspace_bytes(-1, 1, 64, 128) == 0
+
+
+def _mask_stride(nb=16):
+    return (ctypes.c_int64 * 3)(16 * nb, 16 * nb, nb)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dropout_p=0.1), ofa.Status.INVALID_ARG),                                  # p without a mask
+    (dict(dropout_mask=0x100000, dropout_p=1.0), ofa.Status.INVALID_ARG),           # p outside [0, 1)
+    (dict(dropout_mask=0x100000, dropout_p=-0.1), ofa.Status.INVALID_ARG),
+    (dict(dropout_mask=0x100000, dropout_p=float("nan")), ofa.Status.INVALID_ARG),
+    (dict(dropout_mask=0x100000, dropout_p=0.1,
+          dropout_mask_stride=(ctypes.c_int64 * 3)(256, 16, -16)), ofa.Status.INVALID_ARG),
+    (dict(dropout_mask=0x100008, dropout_p=0.1), ofa.Status.MISALIGNED),            # base not 16-aligned
+    (dict(dropout_mask=0x100000, dropout_p=0.1,
+          dropout_mask_stride=(ctypes.c_int64 * 3)(256, 16, 8)), ofa.Status.MISALIGNED),
+    (dict(dropout_mask=0x100000, dropout_p=0.1, dk=192), ofa.Status.UNSUPPORTED),   # dk = 192: not built
+])
+def test_fwd_rejects_bad_dropout_arguments_on_the_host(lib, kw, status):
+    kw.setdefault("dropout_mask_stride", _mask_stride())
+    p = _params(**kw)
+    st = lib.attn_fwd(ctypes.byref(p), None)
+    assert st == status, ofa.last_error()
+
+
+def test_decode_and_bwd_refuse_a_dropout_mask(lib):
+    ws = ctypes.c_void_p(0x50000)
+    p = _params(Nq=1, dropout_mask=0x100000, dropout_mask_stride=_mask_stride(), dropout_p=0.1)
+    assert lib.attn_decode_splitkv(ctypes.byref(p), 4, ws, 1 << 20, None) == ofa.Status.UNSUPPORTED
+    b = ofa.BwdParams()
+    b.fwd = _params(Nq=64, Nk=64, dropout_mask=0x100000, dropout_mask_stride=_mask_stride(), dropout_p=0.1)
+    b.fwd.lse = 0x60000
+    for name, addr in (("dout", 0x70000), ("dq", 0x80000), ("dk", 0x90000), ("dv", 0xA0000)):
+        setattr(b, name, addr)
+        setattr(b, name + "_stride", (ctypes.c_int64 * 3)(16 * 128, 128, 128))
+    need = lib.attn_bwd_workspace_bytes(1, 1, 64, 128)
+    assert lib.attn_bwd(ctypes.byref(b), ctypes.c_void_p(0xB0000), need, None) == ofa.Status.UNSUPPORTED

@@ -1,0 +1,91 @@
+"""GPU parity of the dropout forward (keep mask as an input) against the oracle.
+
+The kernels read the bit-packed mask (workloads.pack_keep_mask); the oracle reads the same
+keep decisions unpacked.  Kept weights are scaled by 1 / (1 - p), the row sum and lse are the
+undropped ones; empty rows stay +0.0 / -inf."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import online_softmax_fa2_gb300 as ofa
+from online_softmax_fa2_gb300 import workloads as wl
+from helpers import TOL, compare, cpu32, empty_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run(a, keep, p, **kw):
+    mask = wl.pack_keep_mask(keep)
+    o, lse = ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
+                          scale=a.scale, dropout_mask=mask, dropout_p=p, **kw)
+    torch.cuda.synchronize()
+    assert ofa.device_error_flags() & 1 == 0
+    return o, lse
+
+
+def ref(a, keep, p):
+    return oracle.attn_fwd_dropout(cpu32(a.q), cpu32(a.k), cpu32(a.v), keep.cpu(), p, bias=cpu32(a.bias),
+                                   kv_lens=None if a.kv_lens is None else a.kv_lens.cpu(),
+                                   causal=a.causal, scale=a.scale)
+
+
+@pytest.mark.parametrize("dk,dv,causal,bias,p", [
+    (128, 128, True, False, 0.2),
+    (64, 64, False, True, 0.5),
+    (128, 64, True, False, 0.1),
+    (64, 128, True, True, 0.3),
+])
+def test_bf16_dropout_matches_oracle(dk, dv, causal, bias, p):
+    a = wl.make_prefill(2, 3, 300, 333, dk, dv, torch.bfloat16, causal=causal, bias=bias,
+                        kv_lens=[333, 170], seed=41, device=DEV)
+    keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p, seed=7, device=DEV)
+    o, lse = run(a, keep, p)
+    o_ref, l_ref = ref(a, keep, p)
+    tol = TOL[torch.bfloat16]["o"] / (1.0 - p)  # kept weights are scaled up by 1 / (1 - p)
+    err = float(np.max(np.abs(o.float().cpu().numpy() - o_ref)))
+    assert err <= tol, (err, tol)
+    compare(torch.zeros_like(o), lse, np.zeros_like(o_ref), l_ref, torch.bfloat16, empty=empty_rows(a),
+            what="lse with dropout")
+
+
+def test_bf16_dropout_all_kept_is_bitwise_the_forward():
+    a = wl.make_prefill(2, 2, 260, 260, 128, 128, torch.bfloat16, causal=True, kv_lens=[260, 99],
+                        seed=42, device=DEV)
+    keep = torch.ones((a.B, a.H, a.Nq, a.Nk), dtype=torch.bool, device=DEV)
+    o1, l1 = run(a, keep, 0.0)
+    o0, l0 = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=True, scale=a.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o0.view(torch.int16)) and torch.equal(l1, l0)
+
+
+def test_bf16_dropout_lse_is_the_undropped_one():
+    a = wl.make_prefill(1, 2, 200, 200, 128, 128, torch.bfloat16, causal=True, seed=43, device=DEV)
+    o0, l0 = ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale)
+    keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, 0.6, seed=8, device=DEV)
+    _, l1 = run(a, keep, 0.6)
+    assert torch.equal(l0, l1)
+
+
+def test_fp32_dropout_matches_oracle():
+    a = wl.make_prefill(1, 2, 70, 90, 32, 48, torch.float32, causal=True, kv_lens=[77], seed=44,
+                        device=DEV)
+    keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, 0.25, seed=9, device=DEV)
+    o, lse = run(a, keep, 0.25, block_k=32)
+    o_ref, l_ref = ref(a, keep, 0.25)
+    compare(o, lse, o_ref, l_ref, torch.float32, what="fp32 dropout")
+
+
+def test_bf16_dropout_full_size_sampled_heads():
+    # the 2k causal prefill workload with p = 0.1, two heads checked against the oracle
+    a = wl.causal_2k(DEV)
+    keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, 0.1, seed=10, device=DEV)
+    o, lse = run(a, keep, 0.1)
+    for (b, h) in [(0, 0), (3, 15)]:
+        sub = wl.make_prefill(1, 1, a.Nq, a.Nk, a.dk, a.dv, torch.bfloat16, causal=True, seed=0, device="cpu")
+        sub.q, sub.k, sub.v = (t[b:b + 1, :, h:h + 1].cpu() for t in (a.q, a.k, a.v))
+        o_ref, l_ref = ref(sub, keep[b:b + 1, h:h + 1], 0.1)
+        err = float(np.max(np.abs(o[b, :, h].float().cpu().numpy() - o_ref[0, :, 0])))
+        assert err <= TOL[torch.bfloat16]["o"] / 0.9, (b, h, err)
+        assert float(np.max(np.abs(lse[b, h].cpu().numpy() - l_ref[0, 0]))) <= TOL[torch.bfloat16]["lse"]
