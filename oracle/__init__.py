@@ -207,6 +207,43 @@ def attn_fwd_dropout(q, k, v, keep, p_drop, bias=None, kv_lens=None, causal=Fals
     return o, lse
 
 
+def attn_bwd_dropout(q, k, v, dout, keep, p_drop, bias=None, kv_lens=None, causal=False,
+                     scale=None, lib=None):
+    """Gradients of sum(dout * O) for attn_fwd_dropout's output, in float64 (small inputs only).
+
+    The chain rule through W = keep / (1 - p_drop) * P (P the undropped weights, O = W V):
+    dV = W^T G; the gradient reaching P_ij is keep_ij / (1 - p_drop) * g_i . v_j, and the
+    softmax Jacobian turns it into dS_ij = P_ij (keep_ij / (1 - p_drop) * g_i . v_j - c_i) with
+    c_i = g_i . o_i; dQ = scale * dS K, dK = scale * dS^T Q ("How Does FlashAttention Preserve
+    Global Softmax Across Tiles?", section 7, with the mask its section 6 asks the backward to
+    reproduce).  Returns (dQ [B, Nq, H, dk], dK [B, Nk, H, dk], dV [B, Nk, H, dv])."""
+    if not 0.0 <= p_drop < 1.0:
+        raise ValueError("p_drop must be in [0, 1)")
+    q64, k64, v64 = (_f32(t).astype(np.float64) for t in (q, k, v))
+    g64 = _f32(dout).astype(np.float64)
+    B, H, Nq, Nk, dk, dv = _shapes(_f32(q), _f32(k), _f32(v))
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    kvl = _kvl(kv_lens)
+    if kvl is not None:  # rows past a sequence's key length are no part of any sum
+        for b in range(B):
+            n = min(max(int(kvl[b]), 0), Nk)
+            k64[b, n:] = 0.0
+            v64[b, n:] = 0.0
+    P = attn_probs(q, k, v, bias=bias, kv_lens=kv_lens, causal=causal, scale=scale, lib=lib)
+    keep = np.asarray(keep.cpu().numpy() if hasattr(keep, "cpu") else keep) != 0
+    zs = np.where(keep, 1.0 / (1.0 - p_drop), 0.0)
+    W = P * zs
+    O = np.einsum("bhij,bjhd->bihd", W, v64)
+    dV = np.einsum("bhij,bihd->bjhd", W, g64)
+    GV = np.einsum("bihd,bjhd->bhij", g64, v64)
+    c = np.einsum("bihd,bihd->bhi", g64, O)
+    dS = P * (zs * GV - c[..., None])
+    dQ = scale * np.einsum("bhij,bjhd->bihd", dS, k64)
+    dK = scale * np.einsum("bhij,bihd->bjhd", dS, q64)
+    return dQ, dK, dV
+
+
 def key_state(q, k, v, j0, j1, bias=None, kv_lens=None, causal=False, scale=None,
               lib=None):
     """State (m, l, u) of every row over the visible keys in [j0, j1): [B, H, Nq, 2 + dv]."""

@@ -100,3 +100,63 @@ def test_packed_mask_round_trip():
     bits = np.unpackbits(packed.numpy(), axis=-1, bitorder="little")
     assert np.array_equal(bits[..., :300].astype(bool), keep.numpy())
     assert not bits[..., 300:].any()
+
+
+# ---- backward of the dropout forward
+
+
+def grads(a, keep, p, dout):
+    return oracle.attn_bwd_dropout(a.q, a.k, a.v, dout, keep, p, kv_lens=a.kv_lens, causal=a.causal,
+                                   scale=a.scale)
+
+
+def test_bwd_all_kept_no_drop_is_the_backward():
+    a = small(lens=[37, 20], seed=21)
+    dout = torch.randn(a.B, a.Nq, a.H, a.dv, generator=torch.Generator().manual_seed(1))
+    keep = torch.ones((a.B, a.H, a.Nq, a.Nk), dtype=torch.bool)
+    got = grads(a, keep, 0.0, dout)
+    want = oracle.attn_bwd(a.q, a.k, a.v, dout, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale)[:3]
+    for x, y in zip(got, want):
+        assert np.allclose(x, y, rtol=1e-12, atol=1e-12)
+
+
+def test_bwd_none_kept_passes_no_gradient():
+    a = small(lens=[37, 11], seed=22)
+    dout = torch.randn(a.B, a.Nq, a.H, a.dv, generator=torch.Generator().manual_seed(2))
+    keep = torch.zeros((a.B, a.H, a.Nq, a.Nk), dtype=torch.bool)
+    for x in grads(a, keep, 0.4, dout):
+        assert np.all(x == 0.0)
+
+
+def test_bwd_matches_finite_differences_of_the_dropout_forward():
+    # central differences of L = sum(dout * O_drop) in float64, at a few entries of q, k, v
+    a = wl.make_prefill(1, 2, 9, 11, 6, 5, torch.float32, causal=True, kv_lens=[10], seed=23,
+                        device="cpu", poison=False)
+    g = torch.Generator().manual_seed(3)
+    dout = torch.randn(a.B, a.Nq, a.H, a.dv, generator=g).double().numpy()
+    keep = torch.rand((a.B, a.H, a.Nq, a.Nk), generator=g) >= 0.3
+    p = 0.3
+    dQ, dK, dV = grads(a, keep, p, torch.from_numpy(dout))
+    base = {"q": a.q.double().numpy().copy(), "k": a.k.double().numpy().copy(), "v": a.v.double().numpy().copy()}
+
+    def loss(t):
+        o, _ = oracle.attn_fwd_dropout(t["q"], t["k"], t["v"], keep, p, kv_lens=a.kv_lens,
+                                       causal=a.causal, scale=a.scale)
+        return float(np.sum(dout * o))
+
+    # the oracle takes float32 inputs, so a perturbed entry is rounded to float32: a step of
+    # 2^-10 and the 2e-4 of the forward oracle's own finite-difference pin
+    eps = 2.0 ** -10
+    rng = np.random.default_rng(4)
+    for name, grad in (("q", dQ), ("k", dK), ("v", dV)):
+        for _ in range(6):
+            idx = tuple(int(rng.integers(0, s)) for s in base[name].shape)
+            if name in ("k", "v") and idx[1] >= 10:  # past the key length: no part of the loss
+                assert grad[idx] == 0.0
+                continue
+            t1 = {k_: v_.copy() for k_, v_ in base.items()}
+            t2 = {k_: v_.copy() for k_, v_ in base.items()}
+            t1[name][idx] += eps
+            t2[name][idx] -= eps
+            fd = (loss(t1) - loss(t2)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 2e-4 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
