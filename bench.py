@@ -474,6 +474,7 @@ CASES = {
     "decode_nq8": ("decode", {"nq": 8, "causal": True}, "decode"),
     "decode_nq4_b16": ("decode", {"B": 16, "nq": 4, "causal": True}, "decode"),
     "bwd": ("causal_2k", {}, "bwd"),
+    "bwd_dropout": ("causal_2k", {}, "bwd_dropout"),
     "bwd_long": ("long_causal", {"H": 8}, "bwd"),
 }
 
@@ -499,9 +500,13 @@ def run_case(args):
         fn = lambda: ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
                                   scale=a.scale, out=o, lse=lse, dropout_mask=mask, dropout_p=p_drop)
         work, unit = a.flops() / 1e12, "TFLOP/s"
-    elif kind == "bwd":
+    elif kind in ("bwd", "bwd_dropout"):
+        mask, p_drop = None, 0.0
+        if kind == "bwd_dropout":  # the forward's seeded keep mask with p = 0.1
+            p_drop = 0.1
+            mask = wl.pack_keep_mask(wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p_drop, seed=1, device=dev))
         o, lse = ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
-                              scale=a.scale)
+                              scale=a.scale, dropout_mask=mask, dropout_p=p_drop)
         gen = torch.Generator(device=dev)
         gen.manual_seed(7)
         dout = torch.randn(o.shape, generator=gen, device=dev).to(o.dtype)
@@ -509,7 +514,8 @@ def run_case(args):
                          device=dev)
         dq, dk, dv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
         fn = lambda: ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, bias=a.bias, kv_lens=a.kv_lens,
-                                  causal=a.causal, scale=a.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+                                  causal=a.causal, scale=a.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                                  dropout_mask=mask, dropout_p=p_drop)
         # 2 (S) + 2 (dP) + 2 (dV) + 2 (dK) + 2 (dQ) products: (6 dk + 4 dv) FLOPs per visible pair
         work, unit = a.visible_pairs() * (6 * a.dk + 4 * a.dv) / 1e12, "TFLOP/s"
     else:

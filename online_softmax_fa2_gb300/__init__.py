@@ -288,10 +288,11 @@ def bwd_workspace_bytes(B, H, Nq, dk) -> int:
 
 
 def attn_bwd(q, k, v, o, lse, dout, bias=None, kv_lens=None, causal=False, scale=None,
-             dq=None, dk=None, dv=None, workspace=None, stream=None):
+             dq=None, dk=None, dv=None, workspace=None, stream=None, dropout_mask=None, dropout_p=0.0):
     """Gradients (dq, dk, dv) of a loss through o = attn_fwd(q, k, v, ...), given dout = dL/do
-    and the forward's o and lse (bfloat16, dk == dv in {64, 128}).  The mask, bias, kv_lens
-    and causal settings must be the forward's; the bias gets no gradient."""
+    and the forward's o and lse (bfloat16, dk == dv in {64, 128}).  The mask, bias, kv_lens,
+    causal and dropout settings must be the forward's (dropout: dk = dv = 128 without a bias);
+    the bias gets no gradient."""
     lib = load()
     B, Nq, H, d = q.shape
     Nk = k.shape[1]
@@ -305,7 +306,7 @@ def attn_bwd(q, k, v, o, lse, dout, bias=None, kv_lens=None, causal=False, scale
         workspace = torch.empty((max(need, 16) + 3) // 4, dtype=torch.float32, device=q.device)
     _require_cuda(dout, dq, dk, dv, workspace)
     p = BwdParams()
-    p.fwd = make_params(q, k, v, o, lse, bias, kv_lens, causal, scale, 0)
+    p.fwd = make_params(q, k, v, o, lse, bias, kv_lens, causal, scale, 0, dropout_mask, dropout_p)
     p.dout, p.dout_stride = dout.data_ptr(), _bnhd_strides(dout, "dout")
     p.dq, p.dq_stride = dq.data_ptr(), _bnhd_strides(dq, "dq")
     p.dk, p.dk_stride = dk.data_ptr(), _bnhd_strides(dk, "dk")

@@ -129,10 +129,14 @@ __device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
     }
 }
 
+// kDrop: the forward ran with dropout; `dr` holds its keep bits (bit j % 8 of byte j / 8 of a
+// row) and 1 / (1 - p).  The gradient reaching P then carries the mask and its scale: the
+// stored P^T (for dV) is z p / (1 - p), and dS = p (z dP / (1 - p) - c).
+template <bool kDrop>
 __global__ void __launch_bounds__(kTcThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                  const TcArgs a) {
+                  const TcArgs a, const bf16fwd::DropArgs dr) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -360,6 +364,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int it = i0 + 32 * c + lane;
                 Cq[c] = it < a.Nq ? __ldg(c_bh + it) : 0.f;
             }
+            // dropout: lane t holds, for rows 32c + t, the keep bits of this warp's 32 keys
+            uint32_t Zq[4];
+            if constexpr (kDrop) {
+                const uint8_t *zb = dr.dmask + b * dr.dms0 + h * dr.dms1 + (j0 + 32 * (warp & 3)) / 8;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int it = i0 + 32 * c + lane;
+                    Zq[c] = it < a.Nq ? __ldg(reinterpret_cast<const uint32_t *>(zb + (long long)it * dr.dms2)) : 0u;
+                }
+            }
             for (int hh = 0; ok && hh < 2; ++hh) {
             // s_full implies the tile's copies are done; waiting on their barrier as well makes
             // the copied L visible to these threads
@@ -374,6 +388,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // c of row 32c + e is lane e's Cq[c]; L comes from the copy in shared memory (one
                 // broadcast read)
                 const float Ct = Cq[c];
+                uint32_t Zt = 0u;
+                if constexpr (kDrop) Zt = Zq[c];
                 const float *Ls = reinterpret_cast<const float *>(smem + kOffL + (k & 1) * 512) + 32 * c;
                 uint32_t sv[32], dv[32];
                 ptx::tmem_ld32(lane_addr + 32 * c, sv);
@@ -389,7 +405,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float x0, x1, g0, g1;
                     ptx::fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.scale_log2, a.scale_log2,
                               -L2.x, -L2.y);
-                    ptx::add2(g0, g1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -C0, -C1);
+                    float zs0 = 1.f, zs1 = 1.f;  // z / (1 - p) of rows e, e + 1 for this key
+                    if constexpr (kDrop) {
+                        const uint32_t w0 = __shfl_sync(0xffffffffu, Zt, e), w1 = __shfl_sync(0xffffffffu, Zt, e + 1);
+                        zs0 = ((w0 >> lane) & 1u) ? dr.inv_keep : 0.f;
+                        zs1 = ((w1 >> lane) & 1u) ? dr.inv_keep : 0.f;
+                        ptx::fma2(g0, g1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), zs0, zs1, -C0, -C1);
+                    } else {
+                        ptx::add2(g0, g1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -C0, -C1);
+                    }
                     const int i = i0 + 32 * c + e;
                     // visibility of rows i and i + 1 (selects, not products: anything stored past
                     // the sequence, NaN included, is dropped)
@@ -398,7 +422,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const float p0 = v0 ? ptx::ex2(x0) : 0.f, p1 = v1 ? ptx::ex2(x1) : 0.f;
                     float d0, d1;
                     ptx::mul2(d0, d1, p0, p1, g0, g1);
-                    pp[e / 2] = ptx::pack_bf16x2(p0, p1);
+                    if constexpr (kDrop) {  // P^T for dV: the kept, scaled weights
+                        float q0, q1;
+                        ptx::mul2(q0, q1, p0, p1, zs0, zs1);
+                        pp[e / 2] = ptx::pack_bf16x2(q0, q1);
+                    } else {
+                        pp[e / 2] = ptx::pack_bf16x2(p0, p1);
+                    }
                     dp[e / 2] = ptx::pack_bf16x2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
                 }
                 // P^T and dS^T of the half packed into the first 32 of its S^T and dP^T columns
@@ -527,7 +557,12 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     a.dvs0 = p.dv_stride[0]; a.dvs1 = p.dv_stride[1]; a.dvs2 = p.dv_stride[2];
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
-    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    bf16fwd::DropArgs dr;
+    dr.dmask = f.dropout_mask;
+    dr.dms0 = f.dropout_mask_stride[0]; dr.dms1 = f.dropout_mask_stride[1]; dr.dms2 = f.dropout_mask_stride[2];
+    dr.inv_keep = f.dropout_mask ? (float)(1.0 / (1.0 - (double)f.dropout_p)) : 1.f;
+    auto kernel = f.dropout_mask ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     if ((f.Nk + BK - 1) / BK > 65535 || f.B > 65535)
         return fail(ATTN_ERR_UNSUPPORTED, "backward supports B <= 65535 and Nk <= %d", 65535 * BK);
@@ -543,7 +578,7 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel, mq, mk, mv, mg, a);
+    e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mg, a, dr);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward (tcgen05) launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }

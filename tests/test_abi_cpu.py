@@ -175,15 +175,27 @@ def test_fwd_rejects_bad_dropout_arguments_on_the_host(lib, kw, status):
     assert st == status, ofa.last_error()
 
 
-def test_decode_and_bwd_refuse_a_dropout_mask(lib):
+def test_decode_refuses_and_bwd_restricts_a_dropout_mask(lib):
     ws = ctypes.c_void_p(0x50000)
     p = _params(Nq=1, dropout_mask=0x100000, dropout_mask_stride=_mask_stride(), dropout_p=0.1)
     assert lib.attn_decode_splitkv(ctypes.byref(p), 4, ws, 1 << 20, None) == ofa.Status.UNSUPPORTED
-    b = ofa.BwdParams()
-    b.fwd = _params(Nq=64, Nk=64, dropout_mask=0x100000, dropout_mask_stride=_mask_stride(), dropout_p=0.1)
-    b.fwd.lse = 0x60000
-    for name, addr in (("dout", 0x70000), ("dq", 0x80000), ("dk", 0x90000), ("dv", 0xA0000)):
-        setattr(b, name, addr)
-        setattr(b, name + "_stride", (ctypes.c_int64 * 3)(16 * 128, 128, 128))
-    need = lib.attn_bwd_workspace_bytes(1, 1, 64, 128)
-    assert lib.attn_bwd(ctypes.byref(b), ctypes.c_void_p(0xB0000), need, None) == ofa.Status.UNSUPPORTED
+
+    def bp(mask=0x100000, stride=None, **kw):
+        b = ofa.BwdParams()
+        b.fwd = _params(Nq=64, Nk=64, dropout_mask=mask, dropout_mask_stride=stride or _mask_stride(),
+                        dropout_p=0.1, **kw)
+        b.fwd.lse = 0x60000
+        for name, addr in (("dout", 0x70000), ("dq", 0x80000), ("dk", 0x90000), ("dv", 0xA0000)):
+            setattr(b, name, addr)
+            setattr(b, name + "_stride", (ctypes.c_int64 * 3)(16 * 128, 128, 128))
+        return b
+    wsb = ctypes.c_void_p(0xB0000)
+    need = lib.attn_bwd_workspace_bytes(1, 1, 64, 64)
+    # the backward of a dropout forward runs on the d = 128 kernel without a bias only
+    assert lib.attn_bwd(ctypes.byref(bp(dk=64, dv=64)), wsb, need, None) == ofa.Status.UNSUPPORTED
+    b = bp()
+    b.fwd.bias = 0xC0000
+    assert lib.attn_bwd(ctypes.byref(b), wsb, 1 << 20, None) == ofa.Status.UNSUPPORTED
+    assert lib.attn_bwd(ctypes.byref(bp(mask=0x100004)), wsb, 1 << 20, None) == ofa.Status.MISALIGNED
+    assert lib.attn_bwd(ctypes.byref(bp(stride=(ctypes.c_int64 * 3)(256, 16, 4))), wsb, 1 << 20,
+                        None) == ofa.Status.MISALIGNED

@@ -89,3 +89,73 @@ def test_bf16_dropout_full_size_sampled_heads():
         err = float(np.max(np.abs(o[b, :, h].float().cpu().numpy() - o_ref[0, :, 0])))
         assert err <= TOL[torch.bfloat16]["o"] / 0.9, (b, h, err)
         assert float(np.max(np.abs(lse[b, h].cpu().numpy() - l_ref[0, 0]))) <= TOL[torch.bfloat16]["lse"]
+
+
+# ---- backward of the dropout forward (the d = 128 tcgen05 kernel)
+
+BWD_TOL = 2e-2  # bf16 P, dS and gradients: as the plain backward's tests
+
+
+def run_bwd_drop(a, keep, p, seed=0):
+    mask = wl.pack_keep_mask(keep)
+    o, lse = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale,
+                          dropout_mask=mask, dropout_p=p)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(2000 + seed)
+    dout = torch.randn(o.shape, generator=g, device=DEV).to(o.dtype)
+    grads = ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale,
+                         dropout_mask=mask, dropout_p=p)
+    torch.cuda.synchronize()
+    assert ofa.device_error_flags() & 1 == 0
+    return dout, grads
+
+
+def check_grad(got, ref, what):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite"
+    err = float(np.max(np.abs(g - ref)))
+    lim = BWD_TOL * max(1.0, float(np.max(np.abs(ref))))
+    assert err <= lim, f"{what}: max |err| {err:.3e} > {lim:.3e}"
+
+
+@pytest.mark.parametrize("causal,p,lens", [(True, 0.2, [333, 170]), (False, 0.5, [301, 333])])
+def test_bwd_dropout_matches_oracle(causal, p, lens):
+    a = wl.make_prefill(2, 2, 300, 333, 128, 128, torch.bfloat16, causal=causal, kv_lens=lens, seed=45,
+                        device=DEV)
+    keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p, seed=11, device=DEV)
+    dout, grads = run_bwd_drop(a, keep, p)
+    refs = oracle.attn_bwd_dropout(cpu32(a.q), cpu32(a.k), cpu32(a.v), cpu32(dout), keep.cpu(), p,
+                                   kv_lens=a.kv_lens.cpu(), causal=causal, scale=a.scale)
+    for got, ref, name in zip(grads, refs, ("dq", "dk", "dv")):
+        check_grad(got, ref, f"{name} causal={causal} p={p}")
+    # keys past the sequence get +0.0 exactly
+    for t in grads[1:]:
+        bits = t.view(torch.int16).cpu().numpy()
+        assert np.all(bits[1, lens[1]:] == 0)
+
+
+def test_bwd_dropout_all_kept_is_bitwise_the_backward():
+    a = wl.make_prefill(2, 2, 260, 260, 128, 128, torch.bfloat16, causal=True, kv_lens=[260, 99], seed=46,
+                        device=DEV)
+    keep = torch.ones((a.B, a.H, a.Nq, a.Nk), dtype=torch.bool, device=DEV)
+    dout, (dq1, dk1, dv1) = run_bwd_drop(a, keep, 0.0)
+    o, lse = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=True, scale=a.scale)
+    dq0, dk0, dv0 = ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, kv_lens=a.kv_lens, causal=True, scale=a.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dk1.view(torch.int16), dk0.view(torch.int16))
+    assert torch.equal(dv1.view(torch.int16), dv0.view(torch.int16))
+    # dQ is added with atomics in a varying order: equal within its last bits
+    assert (dq1.float() - dq0.float()).abs().max().item() <= 1e-2 * max(1.0, dq0.float().abs().max().item())
+
+
+def test_bwd_dropout_full_size_one_head():
+    # the 2k causal workload with p = 0.1: one (b, h) head against the oracle
+    a = wl.causal_2k(DEV)
+    keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, 0.1, seed=12, device=DEV)
+    dout, grads = run_bwd_drop(a, keep, 0.1, seed=3)
+    b, h = 2, 9
+    sl = lambda t: cpu32(t[b:b + 1, :, h:h + 1])
+    refs = oracle.attn_bwd_dropout(sl(a.q), sl(a.k), sl(a.v), sl(dout), keep[b:b + 1, h:h + 1].cpu(), 0.1,
+                                   causal=True, scale=a.scale)
+    for got, ref, name in zip(grads, refs, ("dq", "dk", "dv")):
+        check_grad(got[b:b + 1, :, h:h + 1], ref, f"{name} full-size head")
