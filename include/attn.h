@@ -106,8 +106,9 @@ typedef enum {
  *                       FlashAttention Preserve Global Softmax Across Tiles?", section 6,
  *                       disables dropout and asks exactly that of a training backward).
  *                       bfloat16: dk <= 128 only, the mask 16-byte aligned with strides that
- *                       are multiples of 16 bytes.  Not taken by attn_decode_splitkv or
- *                       attn_bwd (ATTN_ERR_UNSUPPORTED).
+ *                       are multiples of 16 bytes.  Not taken by attn_decode_splitkv, nor by
+ *                       attn_bwd other than for dk = dv = 128 without a bias
+ *                       (ATTN_ERR_UNSUPPORTED).
  *   dropout_p           in [0, 1) with a mask; must be 0 without one.
  */
 typedef struct {
@@ -247,8 +248,11 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk);
  *  p_ij = exp(x_ij - L_i) tile by tile from Q, K, the fixed mask and bias, takes
  *  c_i = g_i . o_i, dS_ij = p_ij (g_i . v_j - c_i), and accumulates dV_j += p_ij g_i,
  *  dK_j += scale dS_ij q_i, dQ_i += scale dS_ij k_j.)
- * The mask, bias, kv_lens and causal settings must be the forward's.  The bias is fixed: no
- * gradient is formed for it.  An empty row (lse = -inf) passes no gradient, and a key that no
+ * The mask, bias, kv_lens, causal and dropout settings must be the forward's: with a
+ * dropout_mask in fwd (the forward's keep bits and dropout_p) the gradient reaching the
+ * weights carries the mask and the 1 / (1 - p) scale, dV is formed from the kept, scaled
+ * weights, and c_i = g_i . o_i already holds the dropout through o (dk = dv = 128 without a
+ * bias only; otherwise ATTN_ERR_UNSUPPORTED).  The bias is fixed: no gradient is formed for it.  An empty row (lse = -inf) passes no gradient, and a key that no
  * row sees gets dK = dV = 0.
  * Queues three kernels on `stream`: the row terms, the products (on the 5th-generation
  * tensor cores for dk = dv = 128 without a bias, on warp-level tensor-core tiles otherwise),
