@@ -18,7 +18,9 @@
  *       section 3  the state (m, l, u) and the merge of disjoint key subsets;
  *       section 5  tile loop, rows keep their own state, divide once at the end;
  *       section 6  global positions; causal masks align the two sequences' ends
- *                  ("bottom-right"); an entirely empty row returns zero;
+ *                  ("bottom-right"); an entirely empty row returns zero; dropout is
+ *                  disabled there, and a training backward must reproduce the forward's
+ *                  mask and scaling (the keep mask of attn_fwd is therefore an input);
  *       section 7  the saved log-sum-exp L_i, and the backward that rebuilds the
  *                  probabilities from it (attn_bwd);
  *       section 8  decode (one query row, or a few, against a long key/value cache) split
