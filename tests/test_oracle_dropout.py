@@ -160,3 +160,21 @@ def test_bwd_matches_finite_differences_of_the_dropout_forward():
             t2[name][idx] -= eps
             fd = (loss(t1) - loss(t2)) / (2 * eps)
             assert abs(fd - grad[idx]) <= 2e-4 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_mask_bits_under_a_minus_inf_bias_do_not_matter():
+    a = wl.make_prefill(2, 2, 21, 23, 8, 8, torch.float32, causal=False, bias=True, kv_lens=[23, 15],
+                        seed=15, device="cpu", bias_mask_p=0.3)
+    g = torch.Generator().manual_seed(6)
+    keep = torch.rand((a.B, a.H, a.Nq, a.Nk), generator=g) >= 0.25
+    hidden = torch.isinf(a.bias) & (a.bias < 0)
+    assert hidden.any()
+    flipped = torch.where(hidden, ~keep, keep)
+    kw = dict(bias=a.bias, kv_lens=a.kv_lens, causal=False, scale=a.scale)
+    o1, _ = oracle.attn_fwd_dropout(a.q, a.k, a.v, keep, 0.25, **kw)
+    o2, _ = oracle.attn_fwd_dropout(a.q, a.k, a.v, flipped, 0.25, **kw)
+    assert np.array_equal(o1, o2)
+    d1 = oracle.attn_bwd_dropout(a.q, a.k, a.v, torch.ones(a.B, a.Nq, a.H, a.dv), keep, 0.25, **kw)
+    d2 = oracle.attn_bwd_dropout(a.q, a.k, a.v, torch.ones(a.B, a.Nq, a.H, a.dv), flipped, 0.25, **kw)
+    for x, y in zip(d1, d2):
+        assert np.array_equal(x, y)
