@@ -27,8 +27,14 @@
 // products (one thread); warps 4-7 form P^T and dS^T and, at the end, write dK (times scale)
 // and dV; warps 8-11 read each tile's dQ^T from TMEM (one thread per head dimension), turn
 // blocks of 4 rows x 4 dimensions around among 4 lanes, and add scale * dQ to the fp32
-// accumulator with 16-byte reductions (a warp instruction covers 4 whole 128-byte rows).  Every mbarrier wait is bounded as in the
-// forward kernels.
+// accumulator with 16-byte reductions (a warp instruction covers 4 whole 128-byte rows).
+//
+// The grid is (H, B, key blocks), so that with a causal mask the blocks that see the most query
+// tiles are dispatched first.  The kernel is launched with programmatic stream serialization:
+// its CTAs may set up and load K, V, Q and G while the prep kernel drains, and wait for it only
+// where they touch its outputs (lse * log2 e, c, the zeroed dQ accumulator).  With dropout
+// (kDrop) the forward's keep mask scales the gradient reaching P.  Every mbarrier wait is
+// bounded as in the forward kernels.
 #include "fwd_bf16_common.cuh"
 
 namespace attn {
