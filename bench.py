@@ -438,7 +438,7 @@ def run_ours(args):
                      "peak_kind": f"{pk_kind} dense bf16 (burst)",
                      "frac_sustained": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
                      "frac_nominal": achieved / NOMINAL["bf16_tflops"],
-                     "kernel": "fwd_bf16_pair_kernel<128, 128, false>",
+                     "kernel": "fwd_bf16_pair_kernel<128, 128, false, false>",
                      "traffic": profiled_traffic("fwd_bf16_pair_kernel.causal_b4_h16_n2048_d128.md",
                                                  ("fwd_bf16_pair_sm103.cu", "fwd_bf16_common.cuh",
                                                   "sm100_ptx.cuh"))},
