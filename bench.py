@@ -5,15 +5,24 @@
 A step is one attention forward over the bf16 causal workload B=4, H=16, N=2048, d=128
 (scale 1/sqrt(128)), O in bf16 and lse in fp32, inputs resident in HBM.  value = algorithmic
 TFLOP/s: 2*(dk + dv) FLOPs per visible (query, key) pair, causal pairs only, divided by the
-device time of the step (CUDA events on the launching stream; L2 flushed before every timed
-step by writing a 256 MiB buffer outside the timed interval).  The same line carries:
+device time of a step.  Timing: CUDA events on the launching stream around K back-to-back
+steps, the K-step measurement repeated until about a quarter of a second of device time (so
+the clock record holds many samples); consecutive steps read different copies of the inputs,
+rotated over a set larger than L2, so no step finds its inputs in L2 and no flush is needed.
+The same line carries:
   e2e           the same metric with the step's inputs copied host->device from pinned memory
                 and o, lse copied back inside the timed interval;
   roofline      the fused kernel's achieved TFLOP/s against the measured dense-bf16 peak;
+  long_causal   the causal B=1, H=32, N=16384, d=128 workload (one key per row raised by +8),
+                timed the same way, with its own tensor roofline and CPU-oracle baseline;
+  padbias       the padded workload with a bias, B=8, H=8, N=1024, dk=192, dv=128: its
+                roofline is max(FLOPs / tensor peak, algorithmic bytes / HBM peak), bytes-bound;
   decode        split-KV decode on B=64, H=32, L=8192 (kv_len ~ U{1..8192}), d=128, 16 splits:
-                KV GB/s (visible keys only) against the measured HBM peak;
+                KV GB/s (visible keys only) against the measured HBM peak, and against a
+                read-only pass measured in the same run;
+  backward      dQ, dK, dV of the 2k causal workload;
   cpu_baseline  the float64 CPU oracle timed on a bounded sample of the same workload;
-  clocks        SM clocks sampled with nvidia-smi during the timed region.
+  clocks        SM clocks and throttle reasons sampled during the timed regions.
 Under torchrun (N > 1) every rank runs its own replica (weak scaling, no collective on the data
 path); value = total FLOPs of all ranks / the slowest rank's time.
 
@@ -75,22 +84,73 @@ def profiled_traffic(summary, source):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running."""
+    """SM clocks and throttle reasons sampled while running: through NVML (the library
+    nvidia-smi reads) every 2 ms where it loads, otherwise nvidia-smi every 20 ms."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.nvml = None
+        self.samples = []   # (time, sm MHz, max MHz, set of reasons)
+        self.stop_flag = threading.Event()
+        self.source = None
+
+    def _nvml_open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        found = False
+        try:  # the CUDA device's own UUID: NVML may number the GPUs differently
+            import torch
+            uid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+            found = lib.nvmlDeviceGetHandleByUUID(uid.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            found = False
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        if reasons is None:
+            return None
+        return lib, h, reasons
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h, reasons = self.nvml
+        mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
+                  lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                  reasons(h, ctypes.byref(rs)) == 0)
+            if ok:
+                active = {n for n, bit in self.REASON_BITS.items() if rs.value & bit}
+                self.samples.append((time.time(), float(mhz.value), float(mx.value), active))
+            time.sleep(0.002)
 
     def start(self):
+        self.nvml = self._nvml_open()
+        if self.nvml is not None:
+            self.source = "nvml, every 2 ms"
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.t.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, every 20 ms"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
             time.sleep(0.3)  # nvidia-smi needs a moment before its first sample
@@ -98,41 +158,41 @@ class ClockSampler:
             self.proc = None
 
     def _read(self):
-        for ln in self.proc.stdout:
-            self.lines.append((time.time(), ln.strip()))
-
-    def mark(self):
-        return time.time()
-
-    def stop(self, t0, t1):
-        if not self.proc:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for t, ln in self.lines:
-            if not (t0 - 0.05 <= t <= t1 + 0.05):
-                continue
-            parts = [p.strip() for p in ln.split(",")]
+        for ln in self.proc.stdout:
+            parts = [p.strip() for p in ln.strip().split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(nm)
+            active = {nm for nm, val in zip(names, parts[4:8]) if val.lower().startswith("active")}
+            self.samples.append((time.time(), sm, mx, active))
+
+    def stop(self, windows):
+        """Clock summary over the samples inside the (t0, t1) host-time windows."""
+        self.stop_flag.set()
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.nvml is None and self.proc is None:
+            return None
+        self.t.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        for t, f, m, r in list(self.samples):
+            if any(t0 - 0.005 <= t <= t1 + 0.005 for t0, t1 in windows):
+                sm.append(f)
+                mx.append(m)
+                reasons |= r
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
         sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": sm[len(sm) // 2], "sm_min_mhz": sm[0], "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
 def dist_setup():
@@ -159,33 +219,132 @@ def job_rate(world, units_per_rank, ms, scale=1e12):
     return world * units_per_rank / (ms / 1e3) / scale
 
 
+def head_flops(a, b):
+    """Algorithmic FLOPs of one (b, h) head of workload `a` (visible pairs of sequence b)."""
+    n = a.kv_len_list()[b]
+    if a.causal:
+        pairs = sum(max(0, min(n, i + n - a.Nq + 1)) for i in range(a.Nq))
+    else:
+        pairs = a.Nq * n
+    return pairs * 2 * (a.dk + a.dv)
+
+
 def cpu_oracle_sample(a, seconds_target, seed=0):
-    """Time the float64 oracle on whole heads of workload `a` (taken in a fixed seeded order)
-    until about `seconds_target` of CPU work; returns (TFLOP/s, sample description, threads)."""
+    """Time the float64 oracle on whole (b, h) heads of workload `a`, taken in a fixed seeded
+    order, until about `seconds_target` of CPU work.  Returns (TFLOP/s, seconds, sample
+    description, threads, heads done)."""
     import numpy as np
-    import torch
     import oracle
 
     q = a.q.detach().cpu().float()
     k = a.k.detach().cpu().float()
     v = a.v.detach().cpu().float()
+    bias = None if a.bias is None else a.bias.detach().cpu()
+    lens = a.kv_len_list()
     rng = np.random.default_rng(seed)
     order = rng.permutation(a.B * a.H)
-    flops_head = a.flops() / (a.B * a.H)
-    done, t_used, threads = 0, 0.0, 0
+    done, t_used, threads, flops = 0, 0.0, 0, 0
     while t_used < seconds_target:  # passes over the heads until the time target is reached
         for bh in order:
             b, h = divmod(int(bh), a.H)
+            hb = None if bias is None else bias[b:b + 1, h:h + 1].contiguous()
             t0 = time.perf_counter()
             _, _, threads = oracle.attn_fwd(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, h:h + 1],
-                                            v[b:b + 1, :, h:h + 1], causal=a.causal, scale=a.scale)
+                                            v[b:b + 1, :, h:h + 1], bias=hb,
+                                            kv_lens=None if a.kv_lens is None else [lens[b]],
+                                            causal=a.causal, scale=a.scale)
             t_used += time.perf_counter() - t0
+            flops += head_flops(a, b)
             done += 1
             if t_used >= seconds_target:
                 break
-    return (done * flops_head / t_used / 1e12, t_used,
-            f"{done} head evaluations over the {a.B * a.H} (b, h) heads (whole heads, all causal "
-            f"rows, float64)", threads, done)
+    desc = (f"{done} head evaluations over the {a.B * a.H} (b, h) heads (whole heads, every row, "
+            f"float64)")
+    return flops / t_used / 1e12, t_used, desc, threads, done
+
+
+def cpu_oracle_rows(a, rows, what):
+    """Time the float64 oracle on the flat rows (b*H + h)*Nq + i of workload `a` (no bias).
+    Returns (TFLOP/s over those rows' visible pairs, seconds, sample description, threads)."""
+    import numpy as np
+    import oracle
+
+    q = a.q.detach().cpu().float()
+    k = a.k.detach().cpu().float()
+    v = a.v.detach().cpu().float()
+    lens = a.kv_len_list()
+    rows = np.asarray(rows, np.int64)
+    i = rows % a.Nq
+    b = rows // (a.H * a.Nq)
+    n = np.asarray(lens, np.int64)[b]
+    pairs = np.minimum(n, i + n - a.Nq + 1).clip(min=0) if a.causal else n
+    flops = int(pairs.sum()) * 2 * (a.dk + a.dv)
+    t0 = time.perf_counter()
+    _, _, threads = oracle.attn_fwd(q, k, v, kv_lens=None if a.kv_lens is None else lens,
+                                    causal=a.causal, scale=a.scale, rows=rows)
+    secs = time.perf_counter() - t0
+    return flops / secs / 1e12, secs, f"{rows.size} rows ({what}), {int(pairs.sum())} visible pairs, float64", threads
+
+
+def time_steps(step, steps, stream, min_seconds, est_ms, barrier, clk_windows):
+    """Device time per step of `steps` back-to-back steps (step(s) queues step number s),
+    bracketed by CUDA events on `stream`; the K-step measurement is repeated until about
+    `min_seconds` of device time, the step numbers running on across repeats.  The host-time
+    window of the timed region is appended to `clk_windows`.  Returns (ms per step, repeats)."""
+    import torch
+
+    repeats = max(1, min(1000, math.ceil(min_seconds * 1e3 / max(est_ms * steps, 1e-3))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(repeats)]
+    barrier()
+    t0 = time.time()
+    n = 0
+    for s_, e_ in evs:
+        s_.record(stream)
+        for _ in range(steps):
+            step(n)
+            n += 1
+        e_.record(stream)
+    barrier()
+    clk_windows.append((t0, time.time()))
+    total = sum(s_.elapsed_time(e_) for s_, e_ in evs)
+    return total / (repeats * steps), repeats
+
+
+def warm(step, warmup, stream):
+    """Run `warmup` untimed steps; returns their mean device time in ms (an estimate)."""
+    import torch
+
+    s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step(0)
+    s_.record(stream)
+    for n in range(warmup):
+        step(n)
+    e_.record(stream)
+    torch.cuda.synchronize()
+    return s_.elapsed_time(e_) / max(1, warmup)
+
+
+def rotated_inputs(a, n_sets):
+    """n_sets copies of a workload's inputs with outputs of their own: consecutive steps read
+    different copies, so a step never finds its inputs in L2 when the copies together are
+    larger than L2."""
+    import torch
+
+    sets = []
+    for t in range(n_sets):
+        cp = (lambda x: None if x is None else (x if t == 0 else x.clone()))
+        o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=a.q.device)
+        lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=a.q.device)
+        sets.append((cp(a.q), cp(a.k), cp(a.v), cp(a.bias), o, lse))
+    return sets
+
+
+def set_bytes(a):
+    """Bytes of one input/output set of a forward workload (q, k, v, bias, o, lse)."""
+    t = [a.q, a.k, a.v, a.bias]
+    n = sum(x.numel() * x.element_size() for x in t if x is not None)
+    return n + a.B * a.Nq * a.H * a.dv * a.q.element_size() + a.B * a.H * a.Nq * 4
 
 
 def run_reference(args):
@@ -227,6 +386,47 @@ def run_reference(args):
     return 0
 
 
+def prefill_object(ofa, a, args, stream, pk, pk_kind, clk_windows, barrier, world, dev, n_sets,
+                   roof_kind, traffic):
+    """Time one forward workload (rotated input copies, back-to-back steps) and describe it:
+    value, time per step and roofline ("tensor", or "combined": max(FLOPs / tensor peak,
+    algorithmic bytes / HBM peak))."""
+    sets = rotated_inputs(a, n_sets)
+
+    def step(n):
+        q, k, v, b, o, lse = sets[n % n_sets]
+        ofa.attn_fwd(q, k, v, bias=b, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale, out=o, lse=lse)
+
+    est = warm(step, max(3, args.warmup), stream)
+    ofa.device_error_flags()
+    ms, reps = time_steps(step, args.steps, stream, args.min_seconds, est, barrier, clk_windows)
+    if ofa.device_error_flags() & 1:
+        raise RuntimeError(f"a kernel gave up a bounded wait during the timed region of {a.name}")
+    ms = max_over_ranks(ms, world, dev)
+    flops, nbytes = a.flops(), a.algo_bytes()
+    tflops = job_rate(1, flops, ms)
+    gbs = job_rate(1, nbytes, ms, 1e9)
+    obj = {"workload": a.name, "value": job_rate(world, flops, ms), "unit": "TFLOP/s", "ms_per_step": ms,
+           "steps": args.steps, "repeats": reps, "flops_per_step": flops, "algo_bytes_per_step": nbytes,
+           "gpu_launches_per_step": 1,
+           "l2": f"inputs rotated over {n_sets} copies ({n_sets * set_bytes(a) / 1e6:.0f} MB > 129 MB L2), no flush"}
+    if roof_kind == "tensor":
+        obj["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": tflops / pk["bf16_tflops"], "peak_kind": f"{pk_kind} dense bf16 (burst)",
+                           "frac_nominal": tflops / NOMINAL["bf16_tflops"], "traffic": traffic}
+    else:
+        # bytes-bound: the roofline time is max(FLOPs / tensor peak, bytes / HBM peak)
+        t_tc = flops / (pk["bf16_tflops"] * 1e12)
+        t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+        obj["roofline"] = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "achieved": gbs,
+                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                           "peak_kind": f"{pk_kind} copy bandwidth",
+                           "roofline_ms": 1e3 * max(t_tc, t_hbm), "frac_of_combined": 1e3 * max(t_tc, t_hbm) / ms,
+                           "tensor_frac": tflops / pk["bf16_tflops"], "traffic": traffic}
+    del sets
+    return obj
+
+
 def run_ours(args):
     import torch
     import online_softmax_fa2_gb300 as ofa
@@ -242,46 +442,24 @@ def run_ours(args):
     pk, pk_kind = peaks()
     stream = torch.cuda.current_stream()
 
-    a = wl.causal_2k(dev)
-    flops = a.flops()
-    o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
-    lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale, out=o, lse=lse)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    ofa.device_error_flags()
-
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     clk = ClockSampler(local)
     clk.start()
-    barrier()
-    t0 = time.time()
-    for s, e in ev:
-        flush.zero_()            # L2 flush, outside the timed interval
-        s.record(stream)
-        step()
-        e.record(stream)
-    barrier()
-    t1 = time.time()
-    clocks = clk.stop(t0, t1)
-    ms_steps = [s.elapsed_time(e) for s, e in ev]
-    ms = sum(ms_steps) / len(ms_steps)
-    if ofa.device_error_flags() & 1:
-        raise RuntimeError("a kernel gave up a bounded wait during the timed region")
-    ms = max_over_ranks(ms, world, dev)
+    windows = []          # host-time windows of the headline's timed region
+    other_windows = []    # the other workloads' timed regions
+
+    # ---------------------------------------------------------------- the headline: 2k causal
+    a = wl.causal_2k(dev)
+    flops = a.flops()
+    head_src = ("fwd_bf16_pair_sm103.cu", "fwd_bf16_common.cuh", "sm100_ptx.cuh")
+    head = prefill_object(ofa, a, args, stream, pk, pk_kind, windows, barrier, world, dev, 4, "tensor",
+                          profiled_traffic("fwd_bf16_pair_kernel.causal_b4_h16_n2048_d128.md", head_src))
+    ms = head["ms_per_step"]
     value = job_rate(world, flops, ms)
     achieved = job_rate(1, flops, ms)
 
@@ -292,6 +470,8 @@ def run_ours(args):
     hq = a.q.cpu().pin_memory()
     hk = a.k.cpu().pin_memory()
     hv = a.v.cpu().pin_memory()
+    o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
+    lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
     ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
     hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
     dqkv = [(torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)) for _ in range(2)]
@@ -340,38 +520,78 @@ def run_ours(args):
     ms_e2e = max_over_ranks(ms_e2e, world, dev)
     del dqkv, dout, hq, hk, hv, ho, hl
 
-    # split-KV decode on the long-cache workload (its own roofline: HBM)
+    # ---------------------------------------------------------------- the other prefill workloads
+    extra = {}
+    if not args.no_extra:
+        lc = wl.long_causal(dev)
+        del lc.meta["jstar"]
+        long_src = head_src
+
+        def lc_cpu():
+            import numpy as np
+            # every row of heads 0 and 31, and the last 256 rows of every head
+            whole = np.concatenate([np.arange(lc.Nq) + h * lc.Nq for h in (0, lc.H - 1)])
+            last = np.concatenate([np.arange(lc.Nq - 256, lc.Nq) + h * lc.Nq for h in range(lc.H)])
+            rows = np.unique(np.concatenate([whole, last]))
+            val, secs, desc, threads = cpu_oracle_rows(lc, rows, "every row of heads 0 and 31, the last 256 of every head")
+            return {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
+                    "seconds": secs}
+
+        extra["long_causal"] = prefill_object(
+            ofa, lc, args, stream, pk, pk_kind, other_windows, barrier, world, dev, 2, "tensor",
+            profiled_traffic("fwd_bf16_pair_kernel.causal_b1_h32_n16384_d128.md", long_src))
+        if rank == 0 and not args.no_cpu:
+            extra["long_causal"]["cpu_baseline"] = lc_cpu()
+        del lc
+        pb = wl.padded_bias(dev)
+        extra["padbias"] = prefill_object(
+            ofa, pb, args, stream, pk, pk_kind, other_windows, barrier, world, dev, 3, "combined",
+            profiled_traffic("fwd_bf16_kernel.padbias_b8_h8_n1024_dk192_dv128.md",
+                             ("fwd_bf16_sm103.cu", "fwd_bf16_common.cuh", "sm100_ptx.cuh")))
+        if rank == 0 and not args.no_cpu:
+            val, secs, desc, threads, _ = cpu_oracle_sample(pb, args.cpu_seconds / 2, seed=1)
+            extra["padbias"]["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
+                                                "kind": "oracle", "sample": desc, "seconds": secs}
+        del pb
+
+    # ---------------------------------------------------------------- split-KV decode (HBM)
     dec = None
     if not args.no_decode:
+        # a read-only pass over 4 GiB (torch's sum) as the read bandwidth this run reaches
+        x = torch.ones(1 << 30, dtype=torch.float32, device=dev)
+        x.sum()
+        rs, re_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        rs.record(stream)
+        for _ in range(5):
+            x.sum()
+        re_.record(stream)
+        torch.cuda.synchronize()
+        read_gbs = 5 * x.numel() * 4 / (rs.elapsed_time(re_) / 1e3) / 1e9
+        del x
         d = wl.decode(dev)
         ws = torch.empty(ofa.decode_workspace_bytes(d.B, d.H, d.dv, d.num_splits) // 4,
                          dtype=torch.float32, device=dev)
         od = torch.empty((d.B, 1, d.H, d.dv), dtype=d.q.dtype, device=dev)
         ld = torch.empty((d.B, d.H, 1), dtype=torch.float32, device=dev)
 
-        def dstep():
+        def dstep(n):
             ofa.attn_decode_splitkv(d.q, d.k, d.v, kv_lens=d.kv_lens, num_splits=d.num_splits,
                                     scale=d.scale, workspace=ws, out=od, lse=ld)
 
-        for _ in range(max(3, args.warmup)):
-            dstep()
-        nd = max(5, min(args.steps, 100))
-        barrier()
-        ds, de = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ds.record(stream)
-        for _ in range(nd):       # the 8.6 GB cache is far larger than L2: no flush needed
-            dstep()
-        de.record(stream)
-        barrier()
-        ms_d = max_over_ranks(ds.elapsed_time(de) / nd, world, dev)
+        est = warm(dstep, max(3, args.warmup), stream)
+        # the 8.6 GB cache is far larger than L2: no flush, no copies needed
+        ms_d, reps = time_steps(dstep, args.steps, stream, args.min_seconds, est, barrier, other_windows)
+        ms_d = max_over_ranks(ms_d, world, dev)
         gbs = job_rate(1, d.kv_bytes(), ms_d, 1e9)  # one GPU's rate, against one GPU's peak
         dec = {"workload": "bf16_decode_b64_h32_l8192_d128_splits16",
                "value": job_rate(world, d.kv_bytes(), ms_d, 1e9),
-               "unit": "GB/s", "ms_per_step": ms_d, "steps": nd,
+               "unit": "GB/s", "ms_per_step": ms_d, "steps": args.steps, "repeats": reps,
                "kv_bytes_per_step": d.kv_bytes(), "gpu_launches_per_step": 2,
                "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
                             "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
-                            "peak_kind": f"{pk_kind} copy bandwidth",
+                            "peak_kind": f"{pk_kind} copy bandwidth (read + write)",
+                            "read_peak_gbs": read_gbs, "frac_read": gbs / read_gbs,
+                            "read_peak_kind": "torch sum over 4 GiB, this run (read only)",
                             "frac_nominal": gbs / NOMINAL["hbm_gbs"],
                             "traffic": profiled_traffic("decode_split_kernel.decode_b64_h32_l8192_d128.md",
                                                         ("decode.cu",))}}
@@ -389,6 +609,7 @@ def run_ours(args):
         ws_b = torch.empty(ofa.bwd_workspace_bytes(a.B, a.H, a.Nq, a.dk) // 4 + 4, dtype=torch.float32,
                            device=dev)
         gq, gk, gv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
         def bstep():
             ofa.attn_bwd(a.q, a.k, a.v, o_b, l_b, dout_b, causal=True, scale=a.scale, dq=gq, dk=gk, dv=gv,
@@ -400,12 +621,14 @@ def run_ours(args):
         nb = max(5, min(args.steps, 50))
         evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
         barrier()
+        t0 = time.time()
         for s_, e_ in evb:
             flush.zero_()            # L2 flush, outside the timed interval
             s_.record(stream)
             bstep()
             e_.record(stream)
         barrier()
+        other_windows.append((t0, time.time()))
         if ofa.device_error_flags() & 1:
             raise RuntimeError("a backward kernel gave up a bounded wait during the timed region")
         ms_b = max_over_ranks(sum(s_.elapsed_time(e_) for s_, e_ in evb) / nb, world, dev)
@@ -419,7 +642,18 @@ def run_ours(args):
                             "frac_nominal": tb / NOMINAL["bf16_tflops"],
                             "over": "the whole backward step (bwd_prep_kernel, bwd_tc_kernel, bwd_dq_kernel)",
                             "traffic": None}}
-        del o_b, l_b, dout_b, ws_b, gq, gk, gv
+        del o_b, l_b, dout_b, ws_b, gq, gk, gv, flush
+
+    clocks = clk.stop(windows)
+    clk_all = None
+    if clocks is not None:
+        # the same sampler over every other timed region, for the record
+        sm = [f for t, f, m, r in clk.samples if any(t0 - 0.005 <= t <= t1 + 0.005 for t0, t1 in other_windows)]
+        rs_ = set().union(*[r for t, f, m, r in clk.samples
+                            if any(t0 - 0.005 <= t <= t1 + 0.005 for t0, t1 in other_windows)] or [set()])
+        if sm:
+            sm.sort()
+            clk_all = {"sm_mhz": sm[len(sm) // 2], "sm_min_mhz": sm[0], "reasons": sorted(rs_), "samples": len(sm)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -427,27 +661,26 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": a.B, "H": a.H, "N": a.Nq, "d": a.dk,
-                   "causal": True, "flops_per_step": flops, "l2": "flushed before every step",
+                   "causal": True, "flops_per_step": flops, "l2": head["l2"],
+                   "timing": f"{head['repeats']} repeats of {args.steps} back-to-back steps, CUDA events "
+                             f"around each repeat; ms_per_step = their total / ({head['repeats']} x {args.steps})",
                    "parallelism": f"replicas x{world}"},
-        "gpu_launches": args.steps,
+        "gpu_launches": head["repeats"] * args.steps,
         "e2e": {"value": job_rate(world, flops, ms_e2e), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                 "pipelining": "step k copies in while step k-1 computes and step k-2 copies out"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                     "peak_kind": f"{pk_kind} dense bf16 (burst)",
-                     "frac_sustained": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
-                     "frac_nominal": achieved / NOMINAL["bf16_tflops"],
-                     "kernel": "fwd_bf16_pair_kernel<128, 128, false, false>",
-                     "traffic": profiled_traffic("fwd_bf16_pair_kernel.causal_b4_h16_n2048_d128.md",
-                                                 ("fwd_bf16_pair_sm103.cu", "fwd_bf16_common.cuh",
-                                                  "sm100_ptx.cuh"))},
+        "roofline": dict(head["roofline"],
+                         frac_sustained=achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                         kernel="fwd_bf16_pair_kernel<128, 128, false, false>"),
         "clocks": clocks,
     }
+    line.update(extra)
     if dec:
         line["decode"] = dec
     if bwd is not None:
         line["backward"] = bwd
+    if clk_all:
+        line["clocks_other_regions"] = clk_all
     if rank == 0 and not args.no_cpu:
         val, secs, sample, threads, nheads = cpu_oracle_sample(a, args.cpu_seconds)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
@@ -557,7 +790,10 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true", help="leave out the long causal and padded workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--min-seconds", type=float, default=0.25,
+                    help="device time each timed region is repeated up to (in whole K-step repeats)")
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="time one workload's kernels only (also the command profiled by ncu)")
     args = ap.parse_args()

@@ -190,8 +190,12 @@ attn_status_t attn_decode_splitkv(const attn_fwd_params_t *params, int32_t num_s
  *     (B * H * Nq * num_splits * (2 + dv) * 4 bytes must fit; larger problems return
  *     ATTN_ERR_WORKSPACE and queue nothing).  Every device that loads the library holds that
  *     array until the process exits.  No device memory is allocated by any call.
- *   - The first call on a device looks up the array's device address (with that device
- *     current) and caches it; make that first call before any stream capture.
+ *   - Arguments are checked exactly as attn_decode_splitkv checks them, and before the size
+ *     limit: a bad argument returns its own status, not ATTN_ERR_WORKSPACE.
+ *   - The first call from a CUDA context looks up the array's device address (with the
+ *     device current) and caches it per device, together with that context's unique id; a
+ *     call from a new context (e.g. after cudaDeviceReset) looks it up again.  Make the first
+ *     call on a device, and the first after a reset, before any stream capture.
  *   - All calls share the one array.  Every call writes each partial state it reads, so
  *     nothing needs clearing, but calls whose work overlaps on the GPU (different streams,
  *     several host threads) race on it: order them on one stream.

@@ -162,9 +162,11 @@ extern "C" size_t attn_decode_workspace_bytes(int64_t B, int64_t H, int64_t dv, 
     return attn_decode_workspace_bytes_rows(B, H, 1, dv, num_splits);
 }
 
-extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t num_splits,
-                                             void *workspace, size_t workspace_bytes,
-                                             attn_stream_t stream) {
+namespace attn {
+
+// Every check attn_decode_splitkv makes before it looks at the workspace, in the same order
+// (the allocation-free entry point runs the same ones first).
+attn_status_t check_decode_args(const attn_fwd_params_t *p, int32_t num_splits) {
     g_msg[0] = 0;
     attn_status_t st = check_common(p);
     if (st) return st;
@@ -185,6 +187,17 @@ extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t
     if (!stride_mult(p->q_stride, 8) || !stride_mult(p->k_stride, 8) ||
         !stride_mult(p->v_stride, 8) || !stride_mult(p->o_stride, 8))
         return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
+    return ATTN_OK;
+}
+
+}  // namespace attn
+
+extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t num_splits,
+                                             void *workspace, size_t workspace_bytes,
+                                             attn_stream_t stream) {
+    attn_status_t st = check_decode_args(p, num_splits);
+    if (st) return st;
+    if (p->B * p->H == 0) return ATTN_OK;
     size_t need = attn_decode_workspace_bytes_rows(p->B, p->H, p->Nq, p->dv, num_splits);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)",

@@ -30,6 +30,10 @@ attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t 
 // Largest number of query rows per sequence the split-KV decode takes.
 constexpr int kMaxDecodeRows = 8;
 
+// The argument checks of attn_decode_splitkv that precede its workspace check (clears the
+// last error message first).
+attn_status_t check_decode_args(const attn_fwd_params_t *p, int32_t num_splits);
+
 attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow, float *lrow, cudaStream_t s);
 
 // 4-D TMA map over a bf16 [B, N, H, d] tensor with element strides s (b, n, h); box 64 x 128,

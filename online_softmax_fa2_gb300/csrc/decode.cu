@@ -519,10 +519,44 @@ constexpr size_t kNoAllocScratchBytes = 32u << 20;  // 32 MiB of partial states
 
 static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
 
-// Host code cannot use g_decode_scratch's name as a device address, so the address is looked
-// up once per device (with that device current) and cached.
-void *g_scratch_addr[64];
+// Host code cannot use g_decode_scratch's name as a device address: the address is looked up
+// (cudaGetSymbolAddress, with the device current) the first time a CUDA context calls this
+// entry point, and cached per device together with that context's unique id.  A later call
+// from another context on the same device -- for instance after cudaDeviceReset replaced the
+// primary context -- finds a different id and looks the address up again.
+struct ScratchSlot {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+ScratchSlot g_scratch_slot[64];
 std::mutex g_scratch_mutex;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+bool driver_fn(const char *name, void **fn) {
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+           q == cudaDriverEntryPointSuccess && *fn;
+}
+
+// Unique id of the calling thread's current context, or 0 when there is none yet.
+attn_status_t current_ctx_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *a = nullptr, *b = nullptr;
+        if (!driver_fn("cuCtxGetCurrent", &a) || !driver_fn("cuCtxGetId", &b))
+            return fail(ATTN_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId are not available");
+        get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+        get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuCtxGetCurrent failed");
+    *id = 0;
+    if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuCtxGetId failed");
+    return ATTN_OK;
+}
 
 attn_status_t noalloc_scratch(void **out) {
     int dev = 0;
@@ -530,14 +564,20 @@ attn_status_t noalloc_scratch(void **out) {
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(ATTN_ERR_UNSUPPORTED, "device index %d out of range", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    unsigned long long id = 0;
+    attn_status_t st = current_ctx_id(&id);
+    if (st) return st;
+    ScratchSlot &slot = g_scratch_slot[dev];
+    if (!slot.ptr || id == 0 || slot.ctx_id != id) {
         void *ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
         if (e != cudaSuccess)
             return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-        g_scratch_addr[dev] = ptr;
+        if ((st = current_ctx_id(&id))) return st;  // the lookup may have made the context current
+        slot.ptr = ptr;
+        slot.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.ptr;
     return ATTN_OK;
 }
 
@@ -547,17 +587,18 @@ attn_status_t noalloc_scratch(void **out) {
 extern "C" attn_status_t attn_decode_splitkv_noalloc(const attn_fwd_params_t *p, int32_t num_splits,
                                                      attn_stream_t stream) {
     using namespace attn;
-    if (p && num_splits >= 1) {
-        const size_t need = attn_decode_workspace_bytes_rows(p->B, p->H, p->Nq, p->dv, num_splits);
-        if (need > kNoAllocScratchBytes)
-            return fail(ATTN_ERR_WORKSPACE,
-                        "allocation-free decode needs %zu bytes of partial states for B=%lld H=%lld "
-                        "Nq=%lld dv=%lld num_splits=%d; its built-in scratch holds %zu",
-                        need, (long long)p->B, (long long)p->H, (long long)p->Nq, (long long)p->dv, num_splits,
-                        kNoAllocScratchBytes);
-    }
-    void *scratch = nullptr;
-    attn_status_t st = noalloc_scratch(&scratch);
+    // the workspace entry point's own checks first, so that a bad argument is reported as such
+    attn_status_t st = check_decode_args(p, num_splits);
     if (st) return st;
+    const size_t need = attn_decode_workspace_bytes_rows(p->B, p->H, p->Nq, p->dv, num_splits);
+    if (need > kNoAllocScratchBytes)
+        return fail(ATTN_ERR_WORKSPACE,
+                    "allocation-free decode needs %zu bytes of partial states for B=%lld H=%lld "
+                    "Nq=%lld dv=%lld num_splits=%d; its built-in scratch holds %zu",
+                    need, (long long)p->B, (long long)p->H, (long long)p->Nq, (long long)p->dv, num_splits,
+                    kNoAllocScratchBytes);
+    if (p->B * p->H == 0) return ATTN_OK;
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch))) return st;
     return attn_decode_splitkv(p, num_splits, scratch, kNoAllocScratchBytes, stream);
 }

@@ -156,7 +156,7 @@ __device__ __forceinline__ float tile_logits(float (&x)[BK], float c, int kv0, b
     return mt;
 }
 
-// New reference maximum for a row ("choose the new maximum"): the first visible key sets it
+// The reference maximum of a row: the first visible key sets it
 // (the old state has no mass, so nothing is rescaled); afterwards it moves only when the tile
 // maximum exceeds it by more than kRescaleThreshold, and then alpha = 2^(m_old - m_new).
 __device__ __forceinline__ float update_max(float mt, float &m_run, bool &rescale) {

@@ -80,6 +80,14 @@ class Attn:
         es = torch.tensor([], dtype=self.dtype).element_size()
         return sum(self.kv_len_list()) * self.H * (self.dk + self.dv) * es
 
+    def algo_bytes(self) -> int:
+        """Bytes a forward must move at the least: q, the key and value rows of each sequence's
+        key length, the bias at visible positions (fp32), o, and lse (fp32)."""
+        es = torch.tensor([], dtype=self.dtype).element_size()
+        q_o = self.B * self.Nq * self.H * (self.dk + self.dv) * es
+        bias = 4 * self.visible_pairs() if self.bias is not None else 0
+        return q_o + self.kv_bytes() + bias + 4 * self.B * self.H * self.Nq
+
 
 def _gen(device, seed):
     g = torch.Generator(device=device)

@@ -6,8 +6,9 @@ imports it and shares no code with it.
 
 ``attn_oracle.c`` holds the arithmetic (the plain definition of the operator, row by row,
 in float64); this module compiles it with gcc on first use and wraps it with ctypes.
-``online_ref`` holds a pure-Python restatement of the tiled (m, l, u) recurrence used to
-pin the definition against the pages' own online formulation.
+``online_ref`` holds a pure-Python restatement of the online method as a merge of per-key-set
+(m, l, u) states over any partition of the keys, used to pin the definition against the
+method's own claim that the pieces combine to the whole.
 
 Readings of the pages that the oracle takes (bias not scaled; bottom-right causal aligned
 to each sequence's own key length; bias -inf masks; empty row -> o = +0.0, lse = -inf) are

@@ -98,3 +98,76 @@ def compare_rows(o_s, l_s, o_ref, l_ref, dtype, what=""):
     assert err_o <= tol["o"], f"{what}: max |o - oracle| = {err_o:.3e}"
     assert err_l <= tol["lse"], f"{what}: max |lse - oracle| = {err_l:.3e}"
     return err_o, err_l
+
+
+# Gradient bound of the bf16 backward.  The kernels round P and dS to bf16 before the products
+# that form dV, dK and dQ (a relative error of at most 2^-9 per term), accumulate in fp32 and
+# store the gradients in bf16 (2^-9 again).  An element of a gradient is a sum over rows or
+# keys of such rounded terms whose errors have random signs, so its error is about 2^-9 times
+# the root sum of squares of the terms, which is of the size of the gradient row it belongs
+# to; the stored value adds 2^-9 of the element itself.  One more error does not cancel:
+# c_i = dO_i . O_i is formed from the O the forward stored in bf16 (its rounding, 2^-9, plus
+# the forward's own error of the same order), so |dc_i| <= 2^-8 sum_c |dO_ic O_ic|, and since
+# the weights of a row sum to 1 that error reaches dQ_i as -scale dc_i sum_j p_ij k_j, at most
+# scale |dc_i| max_j |k_jd| in dimension d.  It matters where dQ_i itself nearly cancels (a row
+# that sees one or two keys).  A backward that rounds exactly where the kernels round
+# (tests/test_grad_bound.py) stays under 0.031 x the row's RMS beyond 2^-6 |ref| and the c
+# term, with a relative Frobenius error of 2.2e-3 to 2.8e-3 per tensor.  The bound keeps a
+# margin of 2 to 4 over both:
+#   |g - ref| <= GRAD_RTOL |ref| + GRAD_ATOL_ROW rms(ref row) + (dQ only) the c term
+#   ||g - ref|| / ||ref|| <= GRAD_FRO
+# where a "row" is the head-dimension vector of one query (dQ) or one key (dK, dV) of one
+# (b, h).
+GRAD_RTOL = 2.0 ** -6
+GRAD_ATOL_ROW = 2.0 ** -4
+GRAD_FRO = 1e-2
+
+
+def dq_c_term(dout, o, k, scale, kv_lens=None):
+    """[B, Nq, H, dk] float64: the part of the dQ bound that the bf16 O's rounding in
+    c_i = dO_i . O_i can reach (see above).  dout, o [B, Nq, H, dv]; k [B, Nk, H, dk]; keys
+    past kv_lens (or non-finite) are left out of the maximum."""
+    def arr(t):
+        return t.detach().float().cpu().numpy().astype(np.float64) if torch.is_tensor(t) else np.asarray(t, np.float64)
+    g, oo, kk = arr(dout), arr(o), arr(k)
+    dc = 2.0 ** -8 * np.sum(np.abs(g * oo), axis=-1, keepdims=True)        # [B, Nq, H, 1]
+    ak = np.where(np.isfinite(kk), np.abs(kk), 0.0)
+    if kv_lens is not None:
+        lens = [int(x) for x in (kv_lens.tolist() if torch.is_tensor(kv_lens) else kv_lens)]
+        for b, n in enumerate(lens):
+            ak[b, max(0, n):] = 0.0
+    kmax = ak.max(axis=1, initial=0.0)[:, None]                          # [B, 1, H, dk]
+    return scale * dc * kmax
+
+
+def grad_bound_violations(got, ref, extra=None):
+    """(number of elements over the per-element bound, relative Frobenius error) of a gradient
+    `got` against the float64 `ref`, both [..., d] (got may be a bf16 tensor or an array);
+    `extra` (broadcastable to ref) is added to the per-element limit (the dQ c term)."""
+    g = got.detach().float().cpu().numpy().astype(np.float64) if torch.is_tensor(got) else np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if r.size == 0:
+        return 0, 0.0
+    err = np.abs(g - r)
+    rms_row = np.sqrt(np.mean(r * r, axis=-1, keepdims=True))
+    lim = GRAD_RTOL * np.abs(r) + GRAD_ATOL_ROW * rms_row
+    if extra is not None:
+        lim = lim + extra
+    nref = float(np.linalg.norm(r))
+    fro = float(np.linalg.norm(g - r)) / nref if nref > 0 else float(np.linalg.norm(g))
+    bad = int(np.count_nonzero(~(err <= lim)))
+    return bad, fro
+
+
+def check_grad(got, ref, what, zero=None, extra=None):
+    """Gradient parity within the bound above; `zero` [B, N] marks rows (keys or query rows)
+    that must be +0.0 bit for bit; `extra` is the dQ c term (dq_c_term) for dQ."""
+    g = got.detach().float().cpu().numpy()
+    assert np.all(np.isfinite(g)), f"{what}: non-finite"
+    bad, fro = grad_bound_violations(got, ref, extra)
+    assert bad == 0, f"{what}: {bad} elements over the per-element gradient bound (relative Frobenius {fro:.2e})"
+    assert fro <= GRAD_FRO, f"{what}: relative Frobenius error {fro:.3e} > {GRAD_FRO}"
+    if zero is not None:
+        bits = got.detach().cpu().view(torch.int16).numpy()
+        assert np.all(bits[zero] == 0), f"{what}: rows that must be +0.0 are not"

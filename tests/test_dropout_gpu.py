@@ -10,7 +10,7 @@ import torch
 import oracle
 import online_softmax_fa2_gb300 as ofa
 from online_softmax_fa2_gb300 import workloads as wl
-from helpers import TOL, compare, cpu32, empty_rows
+from helpers import TOL, check_grad, compare, cpu32, dq_c_term, empty_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -93,9 +93,6 @@ def test_bf16_dropout_full_size_sampled_heads():
 
 # ---- backward of the dropout forward (the d = 128 tcgen05 kernel)
 
-BWD_TOL = 2e-2  # bf16 P, dS and gradients: as the plain backward's tests
-
-
 def run_bwd_drop(a, keep, p, seed=0):
     mask = wl.pack_keep_mask(keep)
     o, lse = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale,
@@ -107,15 +104,8 @@ def run_bwd_drop(a, keep, p, seed=0):
                          dropout_mask=mask, dropout_p=p)
     torch.cuda.synchronize()
     assert ofa.device_error_flags() & 1 == 0
+    run_bwd_drop.last_o = o
     return dout, grads
-
-
-def check_grad(got, ref, what):
-    g = got.float().cpu().numpy().astype(np.float64)
-    assert np.all(np.isfinite(g)), f"{what}: non-finite"
-    err = float(np.max(np.abs(g - ref)))
-    lim = BWD_TOL * max(1.0, float(np.max(np.abs(ref))))
-    assert err <= lim, f"{what}: max |err| {err:.3e} > {lim:.3e}"
 
 
 @pytest.mark.parametrize("causal,p,lens", [(True, 0.2, [333, 170]), (False, 0.5, [301, 333])])
@@ -126,8 +116,9 @@ def test_bwd_dropout_matches_oracle(causal, p, lens):
     dout, grads = run_bwd_drop(a, keep, p)
     refs = oracle.attn_bwd_dropout(cpu32(a.q), cpu32(a.k), cpu32(a.v), cpu32(dout), keep.cpu(), p,
                                    kv_lens=a.kv_lens.cpu(), causal=causal, scale=a.scale)
+    ct = dq_c_term(dout, run_bwd_drop.last_o, a.k, a.scale, a.kv_lens)
     for got, ref, name in zip(grads, refs, ("dq", "dk", "dv")):
-        check_grad(got, ref, f"{name} causal={causal} p={p}")
+        check_grad(got, ref, f"{name} causal={causal} p={p}", extra=ct if name == "dq" else None)
     # keys past the sequence get +0.0 exactly
     for t in grads[1:]:
         bits = t.view(torch.int16).cpu().numpy()
@@ -157,5 +148,6 @@ def test_bwd_dropout_full_size_one_head():
     sl = lambda t: cpu32(t[b:b + 1, :, h:h + 1])
     refs = oracle.attn_bwd_dropout(sl(a.q), sl(a.k), sl(a.v), sl(dout), keep[b:b + 1, h:h + 1].cpu(), 0.1,
                                    causal=True, scale=a.scale)
+    ct = dq_c_term(sl(dout), sl(run_bwd_drop.last_o), sl(a.k), a.scale)
     for got, ref, name in zip(grads, refs, ("dq", "dk", "dv")):
-        check_grad(got[b:b + 1, :, h:h + 1], ref, f"{name} full-size head")
+        check_grad(got[b:b + 1, :, h:h + 1], ref, f"{name} full-size head", extra=ct if name == "dq" else None)

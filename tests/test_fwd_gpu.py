@@ -238,9 +238,12 @@ def test_padbias_b8_h8_n1024_dk192_dv128():
 def test_long_causal_b1_h32_n16384_d128():
     a = wl.long_causal(DEV)
     o, lse = run(a)
+    # every row of heads 0 and 31, the last 256 rows of every head (where the lazy rescale
+    # has run longest and most +8 keys were met), and a seeded sample of each head
     rows = sample_rows(a, n_per_head=48, heads=[(0, h) for h in range(a.H)])
-    last = np.concatenate([np.arange(a.Nq - 16, a.Nq) + h * a.Nq for h in range(a.H)])
-    rows = np.unique(np.concatenate([rows, last]))
+    whole = np.concatenate([np.arange(a.Nq) + h * a.Nq for h in (0, a.H - 1)])
+    last = np.concatenate([np.arange(a.Nq - 256, a.Nq) + h * a.Nq for h in range(a.H)])
+    rows = np.unique(np.concatenate([rows, whole, last]))
     o_ref, l_ref, _ = oracle_full(a, rows=rows)
     o_s, l_s = gather_rows(o, lse, rows, a.H, a.Nq)
     compare_rows(o_s, l_s, o_ref, l_ref, torch.bfloat16, what="long causal")

@@ -4,7 +4,7 @@ Every check here runs on the CPU (no GPU, no CUDA library).  Each one pins the o
 something other than itself: a value a page prints for a worked example (fixtures under
 tests/golden/, each with its source), a closed form, an invariant, a special case that a
 library routine computes independently (torch's float64 math attention), or the pages'
-own online recurrence restated in pure Python.
+own merge of per-key-set states restated in pure Python.
 """
 import itertools
 import json
@@ -365,7 +365,7 @@ def test_row_subset_equals_full():
         assert np.array_equal(os_[t], o[bb, i, h]) and (ls_[t] == lse[bb, h, i])
 
 
-# ---------------------------------------------------------------- online recurrence (page 1 s9)
+# ------------------------------------------------- merge of per-piece states (page 1 s3, s4, s9)
 
 def _tol_ok(x, y):
     x, y = np.asarray(x, np.float64), np.asarray(y, np.float64)
@@ -382,7 +382,7 @@ def _tol_ok_inner(x, y):
     return bool(np.all(d <= lim))
 
 
-def _online_vs_oracle(q, k, v, causal, kv_len, tiles, allowed=None, bias=None, scale=None):
+def _online_vs_oracle(q, k, v, causal, kv_len, tiles, allowed=None, bias=None, scale=None, tree=False):
     """q [Nq, dk], k [Nk, dk], v [Nk, dv] for one head; returns True if they agree."""
     nq, nk = q.shape[0], k.shape[0]
     sc = 1.0 / math.sqrt(q.shape[1]) if scale is None else scale
@@ -391,7 +391,7 @@ def _online_vs_oracle(q, k, v, causal, kv_len, tiles, allowed=None, bias=None, s
     o_on, lse_on, _ = online_ref.online_rows(q.astype(np.float64).tolist(),
                                              k.astype(np.float64).tolist(),
                                              v.astype(np.float64).tolist(), tiles, vis, sc,
-                                             bias=bfun, dv=v.shape[1])
+                                             bias=bfun, dv=v.shape[1], tree=tree)
     bias4 = None
     if bias is not None or allowed is not None:
         bb = np.zeros((nq, nk), np.float32) if bias is None else bias.astype(np.float32).copy()
@@ -442,7 +442,8 @@ def test_online_families_agree_with_oracle(family, shape, causal, pad):
     if family.startswith("common"):
         bias = (nrng.standard_normal((nq, nk)) * 300.0).astype(np.float32)  # wide span
     for tiles in _partitions(nk, rng, 6):
-        assert _online_vs_oracle(q, k, v, causal, kv_len, tiles, bias=bias), (family, tiles)
+        for tree in (False, True):  # pieces combined one after another, and as a merge tree
+            assert _online_vs_oracle(q, k, v, causal, kv_len, tiles, bias=bias, tree=tree), (family, tiles)
     if family.startswith("common"):
         assert _online_vs_oracle(q, k, v, causal, kv_len, [list(range(nk))],
                                  bias=bias + np.float32(1000.0))
