@@ -2,8 +2,9 @@
 
 Tolerance: the backward forms P and dS in bf16 for the tensor cores and writes bf16
 gradients; every element is held to |g - ref| <= 2^-6 |ref| + 2^-4 rms(its row) +
-2^-7 rms(tensor), and every tensor to a relative Frobenius error of 1e-2 (helpers.check_grad,
-which derives both from the rounding and calibrates them against a bf16-rounding emulation).
+2^-10 rms(tensor) (plus, for dQ, the reach of the bf16 O through c), and every tensor to a
+relative Frobenius error of 1e-2 (helpers.check_grad, which derives both from the rounding and
+calibrates them against a bf16-rounding emulation).
 What the masks fix is exact: a key that no row sees gets dK = dV = +0.0, and an empty row gets
 dQ = +0.0."""
 import math

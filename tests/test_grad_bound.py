@@ -1,8 +1,8 @@
 """The gradient bound of the GPU backward tests, checked on the CPU against both of its sides.
 
-helpers.check_grad holds each gradient element to 2^-6 |ref| + 2^-4 rms(its row), plus for
-dQ the reach of the bf16 O's rounding through c_i = dO_i . O_i (helpers.dq_c_term), and each
-tensor to a relative Frobenius error of 1e-2.  Here:
+helpers.check_grad holds each gradient element to 2^-6 |ref| + 2^-4 rms(its row) +
+2^-10 rms(tensor), plus for dQ the reach of the bf16 O's rounding through c_i = dO_i . O_i
+(helpers.dq_c_term), and each tensor to a relative Frobenius error of 1e-2.  Here:
   - a backward that rounds exactly where the kernels round (P and dS to bf16 before the
     products, c from the bf16 O, the gradients stored in bf16; torch float32 otherwise)
     passes it on causal, rectangular and non-causal heads, so the bound does not reject
