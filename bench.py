@@ -571,22 +571,34 @@ def run_ours(args):
         d = wl.decode(dev)
         ws = torch.empty(ofa.decode_workspace_bytes(d.B, d.H, d.dv, d.num_splits) // 4,
                          dtype=torch.float32, device=dev)
+        wsf = torch.empty(ofa.decode_fused_workspace_bytes(d.B, d.H, d.dv, d.num_splits) // 4 + 4,
+                          dtype=torch.float32, device=dev)
         od = torch.empty((d.B, 1, d.H, d.dv), dtype=d.q.dtype, device=dev)
         ld = torch.empty((d.B, d.H, 1), dtype=torch.float32, device=dev)
 
-        def dstep(n):
+        def dstep(n):  # two launches: split kernel, then merge kernel
             ofa.attn_decode_splitkv(d.q, d.k, d.v, kv_lens=d.kv_lens, num_splits=d.num_splits,
                                     scale=d.scale, workspace=ws, out=od, lse=ld)
 
-        est = warm(dstep, max(3, args.warmup), stream)
+        def dstep_fused(n):  # one launch: the split kernel's last CTA of each (b, h) merges
+            ofa.attn_decode_splitkv_fused(d.q, d.k, d.v, kv_lens=d.kv_lens, num_splits=d.num_splits,
+                                          scale=d.scale, workspace=wsf, out=od, lse=ld)
+
         # the 8.6 GB cache is far larger than L2: no flush, no copies needed
+        est = warm(dstep_fused, max(3, args.warmup), stream)
+        ms_f, _ = time_steps(dstep_fused, args.steps, stream, args.min_seconds / 2, est, barrier, other_windows)
+        est = warm(dstep, max(3, args.warmup), stream)
         ms_d, reps = time_steps(dstep, args.steps, stream, args.min_seconds, est, barrier, other_windows)
         ms_d = max_over_ranks(ms_d, world, dev)
+        ms_f = max_over_ranks(ms_f, world, dev)
         gbs = job_rate(1, d.kv_bytes(), ms_d, 1e9)  # one GPU's rate, against one GPU's peak
         dec = {"workload": "bf16_decode_b64_h32_l8192_d128_splits16",
                "value": job_rate(world, d.kv_bytes(), ms_d, 1e9),
                "unit": "GB/s", "ms_per_step": ms_d, "steps": args.steps, "repeats": reps,
                "kv_bytes_per_step": d.kv_bytes(), "gpu_launches_per_step": 2,
+               "path": "attn_decode_splitkv (split kernel + merge kernel)",
+               "fused": {"ms_per_step": ms_f, "value": job_rate(world, d.kv_bytes(), ms_f, 1e9),
+                         "path": "attn_decode_splitkv_fused (the last split CTA of each (b, h) merges; one launch)"},
                "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
                             "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                             "peak_kind": f"{pk_kind} copy bandwidth (read + write)",
@@ -595,7 +607,7 @@ def run_ours(args):
                             "frac_nominal": gbs / NOMINAL["hbm_gbs"],
                             "traffic": profiled_traffic("decode_split_kernel.decode_b64_h32_l8192_d128.md",
                                                         ("decode.cu",))}}
-        del d, ws
+        del d, ws, wsf
 
     # backward of the same workload (dQ, dK, dV from o, lse and a seeded random dO): reported
     # beside the forward's line with its own tensor roofline, taken over the whole backward
@@ -702,6 +714,7 @@ CASES = {
     "long_causal": ("long_causal", {}, "fwd"),
     "fp32": ("fp32_small", {}, "fwd"),
     "decode": ("decode", {}, "decode"),
+    "decode_fused": ("decode", {}, "decode_fused"),
     "decode_b16": ("decode", {"B": 16}, "decode"),
     "decode_nq4": ("decode", {"nq": 4, "causal": True}, "decode"),
     "decode_nq8": ("decode", {"nq": 8, "causal": True}, "decode"),
@@ -751,6 +764,15 @@ def run_case(args):
                                   dropout_mask=mask, dropout_p=p_drop)
         # 2 (S) + 2 (dP) + 2 (dV) + 2 (dK) + 2 (dQ) products: (6 dk + 4 dv) FLOPs per visible pair
         work, unit = a.visible_pairs() * (6 * a.dk + 4 * a.dv) / 1e12, "TFLOP/s"
+    elif kind == "decode_fused":
+        ws = torch.empty(ofa.decode_fused_workspace_bytes(a.B, a.H, a.dv, a.num_splits, a.Nq) // 4 + 4,
+                         dtype=torch.float32, device=dev)
+        o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
+        lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
+        fn = lambda: ofa.attn_decode_splitkv_fused(a.q, a.k, a.v, kv_lens=a.kv_lens, bias=a.bias,
+                                                   num_splits=a.num_splits, scale=a.scale,
+                                                   workspace=ws, out=o, lse=lse, causal=a.causal)
+        work, unit = a.kv_bytes() / 1e9, "GB/s"
     else:
         ws = torch.empty(ofa.decode_workspace_bytes(a.B, a.H, a.dv, a.num_splits, a.Nq) // 4,
                          dtype=torch.float32, device=dev)

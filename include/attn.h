@@ -181,6 +181,37 @@ attn_status_t attn_decode_splitkv(const attn_fwd_params_t *params, int32_t num_s
                                   attn_stream_t stream);
 
 /*
+ * Size in bytes of the workspace attn_decode_splitkv_fused needs: the partial states exactly as
+ * for attn_decode_splitkv (attn_decode_workspace_bytes_rows, rounded up to a multiple of 16),
+ * then one 64-bit arrival counter per (b, h), [B, H].  Returns 0 for a negative or zero size.
+ */
+size_t attn_decode_fused_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dv,
+                                         int32_t num_splits);
+
+/*
+ * attn_decode_splitkv_fused -- attn_decode_splitkv in one kernel: the split kernel also does
+ * the merge.  ("How Does FlashAttention Preserve Global Softmax Across Tiles?", section 8:
+ * the extra partial round trip and merge launch of split-KV decode; section 3, the merge.)
+ * Every split CTA writes its partial states, makes them visible device-wide and counts itself
+ * on its (b, h)'s counter; the CTA that counts last merges the S states of every query row of
+ * that (b, h) (the arithmetic of attn_merge_states) and writes o and lse.  No CTA waits for
+ * another.  A counter holds (the call's own tag, count), with a fresh tag for every call, so
+ * a count left by an earlier call, or any other contents, reads as zero.
+ *   - Same arguments, checks and supported shapes as attn_decode_splitkv; same results, bit
+ *     for bit (the same split kernel and the same merge arithmetic).
+ *   - workspace: caller-owned device memory of at least attn_decode_fused_workspace_bytes(...)
+ *     bytes, 16-byte aligned; its contents on entry do not matter.  After the call the
+ *     partial-state part holds the partial states.
+ *   - Calls that share a workspace and overlap on the GPU race on it: order them on a stream.
+ *   - Bit 0 of the device error word is set if a count had to give up (4096 retries of its
+ *     compare-and-swap; with S counting CTAs it retries at most S - 1 times).
+ * Queues one kernel.
+ */
+attn_status_t attn_decode_splitkv_fused(const attn_fwd_params_t *params, int32_t num_splits,
+                                        void *workspace, size_t workspace_bytes,
+                                        attn_stream_t stream);
+
+/*
  * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot allocate device
  * memory when they decode (a framework whose allocator owns the device memory, a plugin
  * handed only its inputs and outputs, a latency-bound loop where cudaMalloc would

@@ -23,7 +23,7 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode_splitkv", "attn_decode_splitkv_noalloc",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode_splitkv", "attn_decode_splitkv_fused", "attn_decode_splitkv_noalloc",
            "attn_merge_states", "decode_workspace_bytes", "bwd_workspace_bytes",
            "device_error_flags", "last_error", "library_path", "load", "AttnError", "Status"]
 
@@ -106,6 +106,10 @@ def load():
         lib.attn_decode_workspace_bytes_rows.restype = ctypes.c_size_t
         lib.attn_decode_splitkv.argtypes = [P, i32, vp, ctypes.c_size_t, vp]
         lib.attn_decode_splitkv.restype = i32
+        lib.attn_decode_fused_workspace_bytes.argtypes = [i64, i64, i64, i64, i32]
+        lib.attn_decode_fused_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_splitkv_fused.argtypes = [P, i32, vp, ctypes.c_size_t, vp]
+        lib.attn_decode_splitkv_fused.restype = i32
         lib.attn_decode_splitkv_noalloc.argtypes = [P, i32, vp]
         lib.attn_decode_splitkv_noalloc.restype = i32
         lib.attn_merge_states.argtypes = [vp, i64, i64, i32, i64, i32, vp,
@@ -261,6 +265,33 @@ def attn_decode_splitkv(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=N
     p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, 0)
     _check(lib.attn_decode_splitkv(ctypes.byref(p), int(num_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse, workspace
+
+
+def decode_fused_workspace_bytes(B, H, dv, num_splits, Nq=1) -> int:
+    return int(load().attn_decode_fused_workspace_bytes(B, H, Nq, dv, num_splits))
+
+
+def attn_decode_splitkv_fused(q, k, v, kv_lens=None, num_splits=16, bias=None, scale=None,
+                              workspace=None, out=None, lse=None, stream=None, causal=False):
+    """Split-KV decode with the merge done by the split kernel (one launch); returns
+    (o, lse, workspace).  The workspace holds the partial states, then one counter per
+    (b, h); its contents on entry do not matter, so the returned workspace can be passed to
+    later calls of any shape that fits."""
+    lib = load()
+    B, Nq, H, _ = q.shape
+    dv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, Nq, H, dv), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    need = decode_fused_workspace_bytes(B, H, dv, num_splits, Nq)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16) + 3) // 4, dtype=torch.float32, device=q.device)
+    _require_cuda(workspace)
+    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, 0)
+    _check(lib.attn_decode_splitkv_fused(ctypes.byref(p), int(num_splits), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse, workspace
 
 

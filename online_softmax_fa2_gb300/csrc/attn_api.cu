@@ -203,10 +203,37 @@ extern "C" attn_status_t attn_decode_splitkv(const attn_fwd_params_t *p, int32_t
         return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)",
                     need, workspace_bytes);
     float *part = static_cast<float *>(workspace);
-    st = launch_decode_split(*p, num_splits, part, reinterpret_cast<cudaStream_t>(stream));
+    st = launch_decode_split(*p, num_splits, part, nullptr, reinterpret_cast<cudaStream_t>(stream));
     if (st) return st;
     return launch_merge(part, p->B, p->H, p->Nq, num_splits, p->dv, p->dtype, p->o, p->o_stride, p->lse,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Partial states (as for attn_decode_splitkv, rounded up to 16 bytes), then B * H counters.
+static size_t fused_counters_offset(int64_t B, int64_t H, int64_t Nq, int64_t dv, int32_t num_splits) {
+    return (attn_decode_workspace_bytes_rows(B, H, Nq, dv, num_splits) + 15) & ~(size_t)15;
+}
+
+extern "C" size_t attn_decode_fused_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dv,
+                                                    int32_t num_splits) {
+    if (B < 0 || H < 0 || Nq < 1 || dv < 1 || num_splits < 1) return 0;
+    return fused_counters_offset(B, H, Nq, dv, num_splits) + (size_t)B * (size_t)H * sizeof(uint64_t);
+}
+
+extern "C" attn_status_t attn_decode_splitkv_fused(const attn_fwd_params_t *p, int32_t num_splits,
+                                                   void *workspace, size_t workspace_bytes,
+                                                   attn_stream_t stream) {
+    attn_status_t st = check_decode_args(p, num_splits);
+    if (st) return st;
+    if (p->B * p->H == 0) return ATTN_OK;
+    const size_t need = attn_decode_fused_workspace_bytes(p->B, p->H, p->Nq, p->dv, num_splits);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(ATTN_ERR_WORKSPACE, "workspace must be 16-byte aligned and hold %zu bytes (got %zu)",
+                    need, workspace_bytes);
+    float *part = static_cast<float *>(workspace);
+    auto *counters = reinterpret_cast<unsigned long long *>(
+        static_cast<char *>(workspace) + fused_counters_offset(p->B, p->H, p->Nq, p->dv, num_splits));
+    return launch_decode_split(*p, num_splits, part, counters, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" attn_status_t attn_merge_states(const float *partials, int64_t B, int64_t H,

@@ -21,8 +21,10 @@ uint32_t *device_flags();
 // Launchers.  Arguments have been validated by the caller (attn_api.cu).
 attn_status_t launch_fwd_f32(const attn_fwd_params_t &p, cudaStream_t s);
 attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s);
+// counters: NULL for the split kernel alone (the merge is a second launch); otherwise the
+// per-(b, h) arrival counters of the fused merge (any contents on entry).
 attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
-                                  cudaStream_t s);
+                                  unsigned long long *counters, cudaStream_t s);
 attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t Nq, int num_splits,
                            int64_t dv, int o_dtype, void *o, const int64_t o_stride[3],
                            float *lse, cudaStream_t s);

@@ -12,6 +12,13 @@
 // pass over the cache: see decode_rows_mma_kernel below.  Partial states are laid out
 // [B, H, Nq, S, 2 + D]; the merge kernel takes one (b, h, row) per CTA.
 //
+// Fused merge (attn_decode_splitkv_fused): every split CTA of a (b, h) writes its states and
+// counts itself on that (b, h)'s counter with a release; the CTA that counts last reads all S
+// states from L2, merges them as the merge kernel does, and writes o and lse.  No CTA waits for another, so one launch does the whole step.  A
+// counter word holds (tag of the call, count): each call has a tag of its own, and a count
+// stored under another tag (an earlier call, or whatever the workspace held) reads as zero,
+// so the workspace needs no clearing.
+//
 // Split kernel (one row): grid (S, H, B), 128 threads.  The cache is read once, with 16-byte loads:
 // a group of D/8 lanes holds one key row (each lane 8 bf16 of K and 8 of V), so a warp
 // reads 32/(D/8) key rows per load instruction, coalesced.  Each group runs the online
@@ -19,6 +26,8 @@
 // 4 keys in flight per group), with the logits kept in base-2 units (x * log2 e) so that one ex2
 // gives each exponential.  The G group states are then merged in shared memory and the
 // split's state is written in natural-log units.
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <mutex>
 
@@ -31,6 +40,17 @@ namespace attn {
 namespace {
 
 using namespace wmma16;
+
+// Tags of fused decode calls: 48 bits, distinct for every call of the process, never 0; the
+// sequence starts from the clock so that it does not repeat an earlier process's.
+unsigned long long next_decode_tag() {
+    static std::atomic<unsigned long long> next{
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull};
+    for (;;) {
+        const unsigned long long t = next.fetch_add(1) & 0xffffffffffffull;
+        if (t) return t;
+    }
+}
 
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -46,7 +66,101 @@ struct DecArgs {
     const int *kv_lens;
     float *part;  // [B, H, Nq, S, 2 + D]
     uint32_t *flags;
+    // fused merge only: per-(b, h) arrival counters (tag << 16 | count), the call's tag, outputs
+    unsigned long long *counters;
+    unsigned long long tag;
+    __nv_bfloat16 *o;
+    long long os0, os1, os2;
+    float *lse;
 };
+
+// Merges the S partial states at st ((m, l, u[0..dv)) each, l == 0: empty) into one output row
+// and its lse (+0.0 and -inf when every part is empty).  One warp: the common maximum M is
+// reduced over the lanes; then, 32 parts at a time, each lane forms one part's weight
+// exp(m_s - M) (0 for an empty part), and the weights are passed round by shuffles while every
+// lane sums weight * u_s over its columns (lane, lane + 32, ... of a block of 256 columns).
+// The states are read from L2 (ld.global.cg), so states that other CTAs wrote during this
+// launch are seen once their writers' fences have been observed.
+template <typename OutT>
+__device__ __forceinline__ void merge_row(const float *st, int S, int dv, OutT *orow, float *lse_out) {
+    const int lane = threadIdx.x & 31, ld = 2 + dv;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32)
+        if (__ldcg(st + s * ld + 1) > 0.f) M = fmaxf(M, __ldcg(st + s * ld));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M == -INFINITY) {
+        for (int c = lane; c < dv; c += 32) orow[c] = OutT(0.f);
+        if (lse_out && lane == 0) *lse_out = -INFINITY;
+        return;
+    }
+    float lsum = 0.f;
+    for (int s = lane; s < S; s += 32) {
+        const float l = __ldcg(st + s * ld + 1);
+        if (l > 0.f) lsum = fmaf(expf(__ldcg(st + s * ld) - M), l, lsum);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = 1.f / lsum;
+    for (int c0 = 0; c0 < dv; c0 += 256) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s = s0 + lane;
+            float w = 0.f;
+            if (s < S && __ldcg(st + s * ld + 1) > 0.f) w = expf(__ldcg(st + s * ld) - M);
+            const int n = min(32, S - s0);
+            for (int i = 0; i < n; ++i) {
+                const float wi = __shfl_sync(0xffffffffu, w, i);
+                if (wi == 0.f) continue;  // uniform across the warp
+                const float *u = st + (s0 + i) * ld + 2 + c0 + lane;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (c0 + lane + 32 * k < dv) acc[k] = fmaf(wi, __ldcg(u + 32 * k), acc[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (c0 + lane + 32 * k < dv) orow[c0 + lane + 32 * k] = OutT(acc[k] * inv);
+    }
+    if (lse_out && lane == 0) *lse_out = M + logf(lsum);
+}
+
+// Fused merge: once every thread's states are written, warp 0 alone stays (the other warps
+// leave, freeing their slots); its lane 0 makes the CTA's states visible device-wide and counts
+// the CTA on its (b, h) counter, and the warp of the last of the S CTAs merges every row of
+// (b, h).  The count is a compare-and-swap on (tag << 16 | count): it retries only when
+// another split of the same (b, h) counted in between (at most S - 1 times), and gives up,
+// reporting through the error word, after 4096.
+template <int D>
+__device__ __forceinline__ void fused_tail(const DecArgs &a, int b, int h) {
+    __syncthreads();  // the CTA's states are written (ordered before lane 0's fence below)
+    if (threadIdx.x >= 32) return;
+    int last = 0;
+    if (threadIdx.x == 0) {
+        __threadfence();  // release: the states, visible device-wide before the count
+        unsigned long long *cnt = a.counters + (long long)b * a.H + h;
+        unsigned long long seen = *reinterpret_cast<volatile unsigned long long *>(cnt), mine = 0;
+        for (int tries = 0;; ++tries) {
+            mine = ((seen >> 16) == a.tag ? (seen & 0xffffull) : 0ull) + 1ull;
+            const unsigned long long prev = atomicCAS(cnt, seen, (a.tag << 16) | mine);
+            if (prev == seen) break;
+            seen = prev;
+            if (tries >= 4096) {
+                atomicOr(a.flags, kFlagWaitTimeout);
+                mine = 0;
+                break;
+            }
+        }
+        last = (mine == (unsigned long long)a.S);
+        if (last) __threadfence();  // acquire: the other splits' states, observed through their counts
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    for (int r = 0; r < a.Nq; ++r) {
+        const long long row = ((long long)b * a.H + h) * a.Nq + r;
+        merge_row<__nv_bfloat16>(a.part + row * a.S * (2 + D), a.S, D,
+                                 a.o + b * a.os0 + r * a.os1 + h * a.os2, a.lse ? a.lse + row : nullptr);
+    }
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -72,7 +186,7 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
 }
 
 // One query row (Nq == 1; with one row the bottom-right causal mask hides no key).
-template <int D>
+template <int D, bool kFuse>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
     constexpr int LPK = D / 8;            // lanes per key row
     constexpr int G = kThreads / LPK;     // key groups per CTA
@@ -175,23 +289,24 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
             out[0] = -INFINITY;
             out[1] = 0.f;
         }
-        return;
-    }
-    float L = 0.f;
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg)
-        if (sm_l[gg] > 0.f) L = fmaf(ex2(sm_m[gg] - M), sm_l[gg], L);
-    for (int c = threadIdx.x; c < D; c += kThreads) {
-        float acc = 0.f;
+    } else {
+        float L = 0.f;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg)
-            if (sm_l[gg] > 0.f) acc = fmaf(ex2(sm_m[gg] - M), sm_u[gg][c], acc);
-        out[2 + c] = acc;
+            if (sm_l[gg] > 0.f) L = fmaf(ex2(sm_m[gg] - M), sm_l[gg], L);
+        for (int c = threadIdx.x; c < D; c += kThreads) {
+            float acc = 0.f;
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg)
+                if (sm_l[gg] > 0.f) acc = fmaf(ex2(sm_m[gg] - M), sm_u[gg][c], acc);
+            out[2 + c] = acc;
+        }
+        if (threadIdx.x == 0) {
+            out[0] = M * kLn2;  // back to natural-log units: exp(x - m) == 2^(x*log2e - M)
+            out[1] = L;
+        }
     }
-    if (threadIdx.x == 0) {
-        out[0] = M * kLn2;  // back to natural-log units: exp(x - m) == 2^(x*log2e - M)
-        out[1] = L;
-    }
+    if constexpr (kFuse) fused_tail<D>(a, b, h);
 }
 
 // ---------------------------------------------------------------- several query rows (Nq >= 2)
@@ -224,7 +339,7 @@ struct RowsLayout {
     static_assert(kRowsWarps * 8 * (2 + D) * 4 <= kBytes, "merge area");
 };
 
-template <int D>
+template <int D, bool kFuse>
 __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
     using L = RowsLayout<D>;
     constexpr int NK = D / 16;  // k-steps of S = Q K^T; 16-dim tiles of O^T
@@ -395,58 +510,35 @@ __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
             out[1] = Lsum;
         }
     }
+    if constexpr (kFuse) fused_tail<D>(a, b, h);
 }
 
-// Merge: one CTA per (b, h, query row i) -- partial-state row (b*H + h)*Nq + i; thread t owns
-// columns t, t + 128, ...
+// Merge: one warp per (b, h, query row i) -- partial-state row (b*H + h)*Nq + i -- four rows
+// per CTA.
 template <typename OutT>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const float *part, int H, int Nq, int S, int dv,
-                                                           OutT *o, long long os0, long long os1,
+__global__ void __launch_bounds__(kThreads) merge_kernel(const float *part, long long rows, int H, int Nq, int S,
+                                                           int dv, OutT *o, long long os0, long long os1,
                                                            long long os2, float *lse) {
-    const long long row = blockIdx.x;
+    const long long row = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
     const int i = (int)(row % Nq), bh = (int)(row / Nq), b = bh / H, h = bh % H;
-    const float *st = part + row * S * (2 + dv);
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) {
-        const float l = st[s * (2 + dv) + 1];
-        if (l > 0.f) M = fmaxf(M, st[s * (2 + dv)]);
-    }
-    OutT *orow = o + b * os0 + i * os1 + h * os2;
-    if (M == -INFINITY) {
-        for (int c = threadIdx.x; c < dv; c += blockDim.x) orow[c] = OutT(0.f);
-        if (lse && threadIdx.x == 0) lse[row] = -INFINITY;
-        return;
-    }
-    float L = 0.f;
-    for (int s = 0; s < S; ++s) {
-        const float l = st[s * (2 + dv) + 1];
-        if (l > 0.f) L = fmaf(expf(st[s * (2 + dv)] - M), l, L);
-    }
-    const float inv = 1.f / L;
-    for (int c = threadIdx.x; c < dv; c += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float *x = st + s * (2 + dv);
-            if (x[1] > 0.f) acc = fmaf(expf(x[0] - M), x[2 + c], acc);
-        }
-        orow[c] = OutT(acc * inv);
-    }
-    if (lse && threadIdx.x == 0) lse[row] = M + logf(L);
+    merge_row<OutT>(part + row * S * (2 + dv), S, dv, o + b * os0 + i * os1 + h * os2, lse ? lse + row : nullptr);
 }
 
-template <int D>
+template <int D, bool kFuse>
 cudaError_t launch_rows(const DecArgs &a, dim3 grid, cudaStream_t st) {
     const int smem = RowsLayout<D>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(decode_rows_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_rows_mma_kernel<D, kFuse>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_rows_mma_kernel<D><<<grid, kThreads, smem, st>>>(a);
+    decode_rows_mma_kernel<D, kFuse><<<grid, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
-                                  cudaStream_t st) {
+                                  unsigned long long *counters, cudaStream_t st) {
     DecArgs a;
     a.B = (int)p.B; a.H = (int)p.H; a.Nk = (int)p.Nk; a.S = num_splits;
     a.Nq = (int)p.Nq; a.causal = p.causal;
@@ -459,6 +551,11 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
     a.vs0 = p.v_stride[0]; a.vs1 = p.v_stride[1]; a.vs2 = p.v_stride[2];
     a.bias = p.bias; a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1]; a.bs2 = p.bias_stride[2];
     a.kv_lens = p.kv_lens; a.part = partials;
+    a.counters = counters;
+    a.tag = counters ? next_decode_tag() : 0ull;
+    a.o = static_cast<__nv_bfloat16 *>(p.o);
+    a.os0 = p.o_stride[0]; a.os1 = p.o_stride[1]; a.os2 = p.o_stride[2];
+    a.lse = p.lse;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     if (p.B > 65535 || p.H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "decode supports B, H <= 65535");
@@ -467,13 +564,19 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
                     (long long)p.Nq);
     dim3 grid((unsigned)num_splits, (unsigned)p.H, (unsigned)p.B);
     cudaError_t e = cudaSuccess;
+    const bool fuse = counters != nullptr;
     if (p.Nq == 1) {
-        if (p.dk == 64) decode_split_kernel<64><<<grid, kThreads, 0, st>>>(a);
-        else decode_split_kernel<128><<<grid, kThreads, 0, st>>>(a);
+        if (p.dk == 64) {
+            if (fuse) decode_split_kernel<64, true><<<grid, kThreads, 0, st>>>(a);
+            else decode_split_kernel<64, false><<<grid, kThreads, 0, st>>>(a);
+        } else {
+            if (fuse) decode_split_kernel<128, true><<<grid, kThreads, 0, st>>>(a);
+            else decode_split_kernel<128, false><<<grid, kThreads, 0, st>>>(a);
+        }
     } else if (p.dk == 64) {
-        e = launch_rows<64>(a, grid, st);
+        e = fuse ? launch_rows<64, true>(a, grid, st) : launch_rows<64, false>(a, grid, st);
     } else {
-        e = launch_rows<128>(a, grid, st);
+        e = fuse ? launch_rows<128, true>(a, grid, st) : launch_rows<128, false>(a, grid, st);
     }
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode rows launch: %s", cudaGetErrorString(e));
     e = cudaGetLastError();
@@ -484,14 +587,15 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
 attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t Nq, int num_splits,
                            int64_t dv, int o_dtype, void *o, const int64_t o_stride[3], float *lse,
                            cudaStream_t st) {
-    if (B * H * Nq > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "B*H*Nq too large");
-    dim3 grid((unsigned)(B * H * Nq));
+    const long long rows = (long long)B * H * Nq;
+    if (rows > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "B*H*Nq too large");
+    dim3 grid((unsigned)((rows + kThreads / 32 - 1) / (kThreads / 32)));
     if (o_dtype == ATTN_DTYPE_BF16)
-        merge_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(partials, (int)H, (int)Nq, num_splits, (int)dv,
+        merge_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, (int)dv,
                                                                static_cast<__nv_bfloat16 *>(o), o_stride[0],
                                                                o_stride[1], o_stride[2], lse);
     else
-        merge_kernel<float><<<grid, kThreads, 0, st>>>(partials, (int)H, (int)Nq, num_splits, (int)dv,
+        merge_kernel<float><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, (int)dv,
                                                        static_cast<float *>(o), o_stride[0], o_stride[1],
                                                        o_stride[2], lse);
     cudaError_t e = cudaGetLastError();

@@ -42,6 +42,21 @@ def test_version_and_workspace_size(lib):
     assert ofa.decode_workspace_bytes(-1, 32, 128, 16) == 0
     assert ofa.decode_workspace_bytes(64, 32, 128, 16, Nq=4) == 4 * 64 * 32 * 16 * 130 * 4
     assert ofa.decode_workspace_bytes(64, 32, 128, 16, Nq=0) == 0
+    # the fused decode: the same partial states (rounded up to 16 bytes), then a uint64 per (b, h)
+    assert ofa.decode_fused_workspace_bytes(64, 32, 128, 16) == 64 * 32 * 16 * 130 * 4 + 64 * 32 * 8
+    assert ofa.decode_fused_workspace_bytes(3, 1, 64, 1) == 16 * ((3 * 66 * 4 + 15) // 16) + 3 * 8
+    assert ofa.decode_fused_workspace_bytes(3, 1, 64, 0) == 0
+
+
+def test_fused_decode_checks_its_workspace_on_the_host(lib):
+    p = _params(Nq=1, Nk=64)
+    need = ofa.decode_fused_workspace_bytes(1, 1, 128, 4)
+    assert lib.attn_decode_splitkv_fused(ctypes.byref(p), 4, ctypes.c_void_p(0x50000), need - 4, None) \
+        == ofa.Status.WORKSPACE
+    assert lib.attn_decode_splitkv_fused(ctypes.byref(p), 4, ctypes.c_void_p(0x50008), need, None) \
+        == ofa.Status.WORKSPACE
+    assert lib.attn_decode_splitkv_fused(ctypes.byref(p), 0, ctypes.c_void_p(0x50000), need, None) \
+        == ofa.Status.INVALID_ARG
 
 
 def _params(**kw):
