@@ -252,6 +252,48 @@ attn_status_t attn_merge_states(const float *partials, int64_t B, int64_t H, int
                                 float *lse, attn_stream_t stream);
 
 /*
+ * attn_fwd_partial -- the state (m, l, u) of every query row over one shard of the keys, for
+ * attention split over the key axis (sequence parallelism across devices, or any split that
+ * the caller merges later).  ("How Does FlashAttention Preserve Global Softmax Across
+ * Tiles?", section 3: the state of a key subset and the merge of disjoint subsets; section 4:
+ * every key in exactly one part; section 6: global positions.)
+ *   params        as for attn_fwd, with k, v (and bias, if any) holding only the shard's keys:
+ *                 params->Nk keys, local key j being global key key_offset + j.  params->o and
+ *                 params->lse are not used (may be NULL).  kv_lens and the causal mask are in
+ *                 global positions: key J of sequence b is visible to row i iff
+ *                 J < min(kv_lens[b], Nk_total) and, when causal, J <= i + n_b - Nq.
+ *   key_offset, Nk_total  the shard [key_offset, key_offset + Nk) of a sequence of Nk_total
+ *                 keys (0 <= key_offset, key_offset + Nk <= Nk_total <= 2^31 - 1).
+ *   partials      device fp32 [B, H, Nq, 2 + dv], 16-byte aligned, written: (m, l, u) with
+ *                 l = sum exp(x_j - m) and u = sum exp(x_j - m) v_j over the shard's visible
+ *                 keys, measured against the row's reference m (natural-log units): the largest
+ *                 visible logit, or a value at most 8 ln 2 below it (the kernel moves its
+ *                 reference only when a larger logit exceeds it by more than that; the merge
+ *                 is the same for any common reference); (-inf, 0, 0...) for a row that sees
+ *                 none of them.
+ * Supported: bfloat16, dk == dv in {64, 128}, with or without a bias; no dropout.  Merging the
+ * states of shards that cover each sequence's keys exactly once (attn_merge_states_rows)
+ * gives attn_fwd's o and lse.  Queues one kernel.
+ */
+attn_status_t attn_fwd_partial(const attn_fwd_params_t *params, int64_t key_offset, int64_t Nk_total,
+                               float *partials, attn_stream_t stream);
+
+/*
+ * attn_merge_states_rows -- attn_merge_states for Nq rows per (b, h) and any layout of the
+ * parts: state s of row r = (b*H + h)*Nq + i is the 2 + dv floats (m, l, u) at
+ * partials + r*row_stride + s*split_stride (strides in floats; 0, 0 mean the decode layout
+ * [B, H, Nq, num_splits, 2 + dv]; states gathered from R devices as [R, B, H, Nq, 2 + dv]
+ * take row_stride = 2 + dv, split_stride = B*H*Nq*(2 + dv)).  Writes o row (b, i, h) at
+ * o + b*o_stride[0] + i*o_stride[1] + h*o_stride[2] (element type o_dtype) and lse [B, H, Nq]
+ * (may be NULL); a row whose parts are all empty gets +0.0 and -inf.  1 <= num_splits <= 4096,
+ * 1 <= dv <= 1024.  Queues one kernel.
+ */
+attn_status_t attn_merge_states_rows(const float *partials, int64_t B, int64_t H, int64_t Nq,
+                                     int32_t num_splits, int64_t dv, int64_t row_stride,
+                                     int64_t split_stride, int32_t o_dtype, void *o,
+                                     const int64_t o_stride[3], float *lse, attn_stream_t stream);
+
+/*
  * Arguments of one attention backward: the forward's arguments and outputs (fwd.o and
  * fwd.lse as the forward wrote them; fwd.lse is required), the upstream gradient of O, and
  * the three gradients to write.

@@ -23,7 +23,8 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode_splitkv", "attn_decode_splitkv_fused", "attn_decode_splitkv_noalloc",
+__all__ = ["attn_fwd", "attn_fwd_partial", "attn_merge_states_rows", "attn_bwd", "attn_decode_splitkv",
+           "attn_decode_splitkv_fused", "attn_decode_splitkv_noalloc",
            "attn_merge_states", "decode_workspace_bytes", "bwd_workspace_bytes",
            "device_error_flags", "last_error", "library_path", "load", "AttnError", "Status"]
 
@@ -115,6 +116,11 @@ def load():
         lib.attn_merge_states.argtypes = [vp, i64, i64, i32, i64, i32, vp,
                                           ctypes.POINTER(ctypes.c_int64), vp, vp]
         lib.attn_merge_states.restype = i32
+        lib.attn_fwd_partial.argtypes = [P, i64, i64, vp, vp]
+        lib.attn_fwd_partial.restype = i32
+        lib.attn_merge_states_rows.argtypes = [vp, i64, i64, i64, i32, i64, i64, i64, i32, vp,
+                                               ctypes.POINTER(ctypes.c_int64), vp, vp]
+        lib.attn_merge_states_rows.restype = i32
         lib.attn_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_bwd.argtypes = [ctypes.POINTER(BwdParams), vp, ctypes.c_size_t, vp]
@@ -236,6 +242,48 @@ def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, block_k
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, block_k, dropout_mask, dropout_p)
     _check(lib.attn_fwd(ctypes.byref(p), _stream(stream)))
+    return out, lse
+
+
+def attn_fwd_partial(q, k, v, key_offset, nk_total, kv_lens=None, bias=None, causal=False, scale=None,
+                     out=None, stream=None):
+    """The state (m, l, u) of every query row over one shard of the keys: k, v (and bias) hold
+    keys [key_offset, key_offset + k.shape[1]) of sequences of nk_total keys; kv_lens and the
+    causal mask are in global positions.  Returns fp32 [B, H, Nq, 2 + dv]."""
+    lib = load()
+    B, Nq, H, _ = q.shape
+    dv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, Nq, 2 + dv), dtype=torch.float32, device=q.device)
+    _require_cuda(out)
+    if out.shape != (B, H, Nq, 2 + dv) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 [B, H, Nq, 2 + dv] tensor")
+    if q.shape[3] != dv:
+        raise ValueError("partial states need dk == dv")
+    # o is not written (q fills the o fields, which the call ignores)
+    p = make_params(q, k, v, q, None, bias, kv_lens, causal, scale, 0)
+    p.o = None
+    _check(lib.attn_fwd_partial(ctypes.byref(p), int(key_offset), int(nk_total), _ptr(out), _stream(stream)))
+    return out
+
+
+def attn_merge_states_rows(partials, B, H, Nq, dv, num_splits, row_stride=0, split_stride=0, out=None,
+                           lse=None, dtype=torch.bfloat16, stream=None):
+    """Merge num_splits states per row (state s of row r = (b*H + h)*Nq + i at
+    partials[r*row_stride + s*split_stride], in floats; 0, 0: the decode layout) into
+    (o [B, Nq, H, dv] of dtype, lse [B, H, Nq])."""
+    lib = load()
+    _require_cuda(partials)
+    if partials.dtype != torch.float32:
+        raise TypeError("partials must be float32")
+    if out is None:
+        out = torch.empty((B, Nq, H, dv), dtype=dtype, device=partials.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=partials.device)
+    os_ = (ctypes.c_int64 * 3)(out.stride(0), out.stride(1), out.stride(2))
+    _check(lib.attn_merge_states_rows(_ptr(partials), int(B), int(H), int(Nq), int(num_splits), int(dv),
+                                      int(row_stride), int(split_stride), _dtype_code(out), _ptr(out), os_,
+                                      _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -255,6 +255,59 @@ extern "C" attn_status_t attn_merge_states(const float *partials, int64_t B, int
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" attn_status_t attn_fwd_partial(const attn_fwd_params_t *p, int64_t key_offset, int64_t Nk_total,
+                                          float *partials, attn_stream_t stream) {
+    g_msg[0] = 0;
+    if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+    attn_fwd_params_t c = *p;  // o is not written: stand partials in for it in the shared checks
+    if (!c.o) c.o = partials;
+    attn_status_t st = check_common(&c);
+    if (st) return st;
+    if (p->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "partial states support bfloat16 only");
+    if (p->dk != p->dv || (p->dk != 64 && p->dk != 128))
+        return fail(ATTN_ERR_UNSUPPORTED, "partial states support dk == dv in {64, 128} (dk=%lld dv=%lld)",
+                    (long long)p->dk, (long long)p->dv);
+    if (p->dropout_mask) return fail(ATTN_ERR_UNSUPPORTED, "partial states take no dropout mask");
+    if (p->block_k != 0) return fail(ATTN_ERR_INVALID_ARG, "block_k must be 0 for bfloat16 (got %d)", p->block_k);
+    if (!(p->scale > 0.0f)) return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path needs scale > 0 (got %g)", p->scale);
+    if (key_offset < 0 || Nk_total < key_offset + p->Nk || Nk_total > INT32_MAX)
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "the shard [key_offset, key_offset + Nk) = [%lld, %lld) must lie in [0, Nk_total = %lld)",
+                    (long long)key_offset, (long long)(key_offset + p->Nk), (long long)Nk_total);
+    if (p->B * p->H * p->Nq == 0) return ATTN_OK;
+    if (!partials || !aligned16(partials)) return fail(ATTN_ERR_MISALIGNED, "partials must be 16-byte aligned");
+    if (!aligned16(p->q) || (p->Nk > 0 && (!aligned16(p->k) || !aligned16(p->v))))
+        return fail(ATTN_ERR_MISALIGNED, "q, k and v must be 16-byte aligned");
+    if (!stride_mult(p->q_stride, 8) || !stride_mult(p->k_stride, 8) || !stride_mult(p->v_stride, 8))
+        return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
+    if (p->bias && (reinterpret_cast<uintptr_t>(p->bias) & 3u))
+        return fail(ATTN_ERR_MISALIGNED, "bias must be 4-byte aligned");
+    return launch_fwd_bf16_partial(*p, key_offset, Nk_total, partials, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" attn_status_t attn_merge_states_rows(const float *partials, int64_t B, int64_t H, int64_t Nq,
+                                                int32_t num_splits, int64_t dv, int64_t row_stride,
+                                                int64_t split_stride, int32_t o_dtype, void *o,
+                                                const int64_t o_stride[3], float *lse, attn_stream_t stream) {
+    g_msg[0] = 0;
+    if (B < 0 || H < 0 || Nq < 0) return fail(ATTN_ERR_INVALID_ARG, "negative B, H or Nq");
+    if (num_splits < 1 || num_splits > 4096)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [1, 4096] (got %d)", num_splits);
+    if (dv < 1 || dv > 1024) return fail(ATTN_ERR_UNSUPPORTED, "dv must be in [1, 1024]");
+    if (row_stride < 0 || split_stride < 0) return fail(ATTN_ERR_INVALID_ARG, "negative state stride");
+    if (o_dtype != ATTN_DTYPE_F32 && o_dtype != ATTN_DTYPE_BF16)
+        return fail(ATTN_ERR_INVALID_ARG, "bad o_dtype %d", o_dtype);
+    if (B * H * Nq == 0) return ATTN_OK;
+    if (!partials || !o || !o_stride) return fail(ATTN_ERR_INVALID_ARG, "partials, o or o_stride is NULL");
+    for (int i = 0; i < 3; ++i)
+        if (o_stride[i] < 0) return fail(ATTN_ERR_INVALID_ARG, "o_stride[%d] is negative", i);
+    // the zero strides stand for the decode layout inside launch_merge: spell them out here
+    const int64_t rs = row_stride ? row_stride : (int64_t)num_splits * (2 + dv);
+    const int64_t ss = split_stride ? split_stride : 2 + dv;
+    return launch_merge(partials, B, H, Nq, num_splits, dv, o_dtype, o, o_stride, lse,
+                        reinterpret_cast<cudaStream_t>(stream), rs, ss);
+}
+
 // dQ accumulator [B, Nq, H, dk], c_i [B, H, Nq], and lse * log2 e [B, H, Nq rounded up to 128]
 // (whole 128-row tiles of it are copied with one bulk copy each), each 16-byte aligned.
 static size_t bwd_ws_parts(int64_t B, int64_t H, int64_t Nq, int64_t dk, size_t *off_c, size_t *off_l) {

@@ -21,13 +21,19 @@ uint32_t *device_flags();
 // Launchers.  Arguments have been validated by the caller (attn_api.cu).
 attn_status_t launch_fwd_f32(const attn_fwd_params_t &p, cudaStream_t s);
 attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s);
+// The forward over one shard of the keys (local key j = global key key_offset + j of Nk_total),
+// writing each row's state (m, l, u) to partials [B, H, Nq, 2 + dv] (fwd_bf16_sm103.cu).
+attn_status_t launch_fwd_bf16_partial(const attn_fwd_params_t &p, int64_t key_offset, int64_t Nk_total,
+                                      float *partials, cudaStream_t s);
 // counters: NULL for the split kernel alone (the merge is a second launch); otherwise the
 // per-(b, h) arrival counters of the fused merge (any contents on entry).
 attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, float *partials,
                                   unsigned long long *counters, cudaStream_t s);
+// State s of row r = (b*H + h)*Nq + i at partials + r*row_stride + s*split_stride (floats);
+// zero strides mean the decode layout [B, H, Nq, S, 2 + dv].
 attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t Nq, int num_splits,
                            int64_t dv, int o_dtype, void *o, const int64_t o_stride[3],
-                           float *lse, cudaStream_t s);
+                           float *lse, cudaStream_t s, int64_t row_stride = 0, int64_t split_stride = 0);
 
 // Largest number of query rows per sequence the split-KV decode takes.
 constexpr int kMaxDecodeRows = 8;

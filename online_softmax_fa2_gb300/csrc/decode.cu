@@ -74,16 +74,18 @@ struct DecArgs {
     float *lse;
 };
 
-// Merges the S partial states at st ((m, l, u[0..dv)) each, l == 0: empty) into one output row
-// and its lse (+0.0 and -inf when every part is empty).  One warp: the common maximum M is
+// Merges the S partial states st, st + ss, st + 2 ss, ... ((m, l, u[0..dv)) each, l == 0:
+// empty) into one output row and its lse (+0.0 and -inf when every part is empty).  One warp: the common maximum M is
 // reduced over the lanes; then, 32 parts at a time, each lane forms one part's weight
 // exp(m_s - M) (0 for an empty part), and the weights are passed round by shuffles while every
 // lane sums weight * u_s over its columns (lane, lane + 32, ... of a block of 256 columns).
 // The states are read from L2 (ld.global.cg), so states that other CTAs wrote during this
 // launch are seen once their writers' fences have been observed.
 template <typename OutT>
-__device__ __forceinline__ void merge_row(const float *st, int S, int dv, OutT *orow, float *lse_out) {
-    const int lane = threadIdx.x & 31, ld = 2 + dv;
+__device__ __forceinline__ void merge_row(const float *st, int S, long long ss, int dv, OutT *orow,
+                                          float *lse_out) {
+    const int lane = threadIdx.x & 31;
+    const long long ld = ss;
     float M = -INFINITY;
     for (int s = lane; s < S; s += 32)
         if (__ldcg(st + s * ld + 1) > 0.f) M = fmaxf(M, __ldcg(st + s * ld));
@@ -157,7 +159,7 @@ __device__ __forceinline__ void fused_tail(const DecArgs &a, int b, int h) {
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     for (int r = 0; r < a.Nq; ++r) {
         const long long row = ((long long)b * a.H + h) * a.Nq + r;
-        merge_row<__nv_bfloat16>(a.part + row * a.S * (2 + D), a.S, D,
+        merge_row<__nv_bfloat16>(a.part + row * a.S * (2 + D), a.S, 2 + D, D,
                                  a.o + b * a.os0 + r * a.os1 + h * a.os2, a.lse ? a.lse + row : nullptr);
     }
 }
@@ -513,16 +515,17 @@ __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
     if constexpr (kFuse) fused_tail<D>(a, b, h);
 }
 
-// Merge: one warp per (b, h, query row i) -- partial-state row (b*H + h)*Nq + i -- four rows
-// per CTA.
+// Merge: one warp per (b, h, query row i) -- row r = (b*H + h)*Nq + i, whose state s sits at
+// part + r * rs + s * ss -- four rows per CTA.
 template <typename OutT>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const float *part, long long rows, int H, int Nq, int S,
-                                                           int dv, OutT *o, long long os0, long long os1,
-                                                           long long os2, float *lse) {
+                                                           long long rs, long long ss, int dv, OutT *o,
+                                                           long long os0, long long os1, long long os2,
+                                                           float *lse) {
     const long long row = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int i = (int)(row % Nq), bh = (int)(row / Nq), b = bh / H, h = bh % H;
-    merge_row<OutT>(part + row * S * (2 + dv), S, dv, o + b * os0 + i * os1 + h * os2, lse ? lse + row : nullptr);
+    merge_row<OutT>(part + row * rs, S, ss, dv, o + b * os0 + i * os1 + h * os2, lse ? lse + row : nullptr);
 }
 
 template <int D, bool kFuse>
@@ -586,18 +589,20 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
 
 attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t Nq, int num_splits,
                            int64_t dv, int o_dtype, void *o, const int64_t o_stride[3], float *lse,
-                           cudaStream_t st) {
+                           cudaStream_t st, int64_t row_stride, int64_t split_stride) {
     const long long rows = (long long)B * H * Nq;
+    const long long rs = row_stride ? row_stride : (long long)num_splits * (2 + dv);
+    const long long ss = split_stride ? split_stride : 2 + dv;
     if (rows > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "B*H*Nq too large");
     dim3 grid((unsigned)((rows + kThreads / 32 - 1) / (kThreads / 32)));
     if (o_dtype == ATTN_DTYPE_BF16)
-        merge_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, (int)dv,
-                                                               static_cast<__nv_bfloat16 *>(o), o_stride[0],
-                                                               o_stride[1], o_stride[2], lse);
+        merge_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, rs, ss,
+                                                               (int)dv, static_cast<__nv_bfloat16 *>(o),
+                                                               o_stride[0], o_stride[1], o_stride[2], lse);
     else
-        merge_kernel<float><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, (int)dv,
-                                                       static_cast<float *>(o), o_stride[0], o_stride[1],
-                                                       o_stride[2], lse);
+        merge_kernel<float><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, rs, ss,
+                                                       (int)dv, static_cast<float *>(o), o_stride[0],
+                                                       o_stride[1], o_stride[2], lse);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
     return ATTN_OK;

@@ -38,22 +38,29 @@ struct Args {
     uint32_t *flags;
 };
 
-// Dropout of a training forward: keep bits (bit j % 8 of byte j / 8 of a row), or null.  A
-// kernel argument of its own, so that the kernels without dropout keep their argument block.
+// Options beyond the plain operator, in a kernel argument of their own so that the kernels
+// that use none keep their argument block (and their register allocation):
+//   dropout of a training forward: keep bits (bit j % 8 of byte j / 8 of a row), or null;
+//   a forward over one shard of the keys (partial states): local key j is global key
+//   key_off + j of a sequence of Nk_tot keys, and part receives each row's (m, l, u).
 struct DropArgs {
     const uint8_t *dmask;
     long long dms0, dms1, dms2;
     float inv_keep;  // 1 / (1 - dropout_p)
+    int key_off, Nk_tot;
+    float *part;
 };
 
-// Key length of sequence b, clamped to [0, Nk] (a clamp is reported once per sequence).
-__device__ __forceinline__ int seq_len(const Args &a, int b, bool report) {
-    if (!a.kv_lens) return a.Nk;
+// Key length of sequence b, clamped to [0, Nk] (a clamp is reported once per sequence); Nk is
+// the whole sequence's key count (a.Nk unless the kernel computes over one shard).
+__device__ __forceinline__ int seq_len(const Args &a, int b, bool report, int Nk) {
+    if (!a.kv_lens) return Nk;
     const int raw = a.kv_lens[b];
-    const int n = min(max(raw, 0), a.Nk);
+    const int n = min(max(raw, 0), Nk);
     if (raw != n && report) atomicOr(a.flags, kFlagKvLenClamped);
     return n;
 }
+__device__ __forceinline__ int seq_len(const Args &a, int b, bool report) { return seq_len(a, b, report, a.Nk); }
 
 // Number of 128-key tiles a query tile starting at row r0 must visit: keys past the last
 // visible key of its last row are never loaded (causal: key j visible to row i iff
@@ -62,6 +69,15 @@ __device__ __forceinline__ int kv_tiles(const Args &a, int r0, int n) {
     if (r0 >= a.Nq) return 0;
     int kv_end = n;
     if (a.causal) kv_end = min(n, max(0, min(r0 + BQ, a.Nq) + n - a.Nq));
+    return (kv_end + BK - 1) / BK;
+}
+
+// The same in a shard's own key numbering: keys j < n are within the sequence and, under the
+// causal mask, key j is visible to row i iff j <= i + shift.
+__device__ __forceinline__ int kv_tiles_shard(const Args &a, int r0, int n, int shift) {
+    if (r0 >= a.Nq) return 0;
+    int kv_end = n;
+    if (a.causal) kv_end = min(n, max(0, min(r0 + BQ, a.Nq) + shift));
     return (kv_end + BK - 1) / BK;
 }
 
@@ -284,6 +300,39 @@ __device__ __forceinline__ void stage_row(uint32_t taddr, float l_run, float m_r
         }
     }
     if (lse_out) *lse_out = empty ? -INFINITY : (m_run + log2f(l_run)) * kLn2;
+}
+
+// The row's state over the keys it saw, to st[0 .. 2 + DV) (skipped when st is null: a row
+// past Nq): m in natural-log units (the base-2 reference m_run times ln 2), the exponential
+// sum l and the unnormalised value sum u, both measured against that reference; (-inf, 0, 0)
+// for a row that saw no key.  st is 8-byte aligned; floats are stored in pairs.  Warp-collective.
+template <int DV>
+__device__ __forceinline__ void write_state(uint32_t taddr, float l_run, float m_run, float *st) {
+    const bool empty = !(l_run > 0.f);
+    float2 *s2 = reinterpret_cast<float2 *>(st);
+    if (st) s2[0] = empty ? make_float2(-INFINITY, 0.f) : make_float2(m_run * kLn2, l_run);
+#pragma unroll
+    for (int cc = 0; cc < DV / 32; ++cc) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(taddr + cc * 32, ov);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(ov);
+        if (st) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                s2[1 + cc * 16 + t] = empty ? make_float2(0.f, 0.f)
+                                            : make_float2(__uint_as_float(ov[2 * t]), __uint_as_float(ov[2 * t + 1]));
+        }
+    }
+}
+
+// The state of a row that sees no key of the kernel's: (-inf, 0, 0).
+template <int DV>
+__device__ __forceinline__ void write_empty_state(float *st) {
+    float2 *s2 = reinterpret_cast<float2 *>(st);
+    s2[0] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int c = 0; c < DV / 2; ++c) s2[1 + c] = make_float2(0.f, 0.f);
 }
 
 // A row that sees no key at all: o = +0.0, lse = -inf (no TMEM involved).

@@ -72,11 +72,15 @@ struct Layout {
 };
 
 // Work item k (0 <= k < B * H * n_items, numbered longest first) -> (b, h, 256-row block).
+// n and shift are in the kernel's own key numbering (a shard's, for partial states): keys
+// j < n lie within the sequence, and under the causal mask key j is visible to row i iff
+// j <= i + shift.
 struct Item {
-    int b, h, q0, n, nA, nB, nmax;
+    int b, h, q0, n, shift, nA, nB, nmax;
 };
 
-__device__ __forceinline__ Item decode_item(const Args &a, int k, bool report) {
+template <bool kShard = false>
+__device__ __forceinline__ Item decode_item(const Args &a, const DropArgs &dr, int k, bool report) {
     Item it;
     const int bhn = a.B * a.H;
     const int blk = a.n_items - 1 - k / bhn;  // later query blocks see more keys: first
@@ -84,9 +88,17 @@ __device__ __forceinline__ Item decode_item(const Args &a, int k, bool report) {
     it.b = bh / a.H;
     it.h = bh % a.H;
     it.q0 = blk * 2 * BQ;
-    it.n = seq_len(a, it.b, report && blk == 0 && it.h == 0);
-    it.nA = kv_tiles(a, it.q0, it.n);
-    it.nB = kv_tiles(a, it.q0 + BQ, it.n);
+    if constexpr (kShard) {
+        const int len = seq_len(a, it.b, report && blk == 0 && it.h == 0, dr.Nk_tot);  // the whole sequence's
+        it.n = min(max(len - dr.key_off, 0), a.Nk);
+        it.shift = len - a.Nq - dr.key_off;
+    } else {  // the whole sequence: no offset
+        const int len = seq_len(a, it.b, report && blk == 0 && it.h == 0);
+        it.n = len;
+        it.shift = len - a.Nq;
+    }
+    it.nA = kv_tiles_shard(a, it.q0, it.n, it.shift);
+    it.nB = kv_tiles_shard(a, it.q0 + BQ, it.n, it.shift);
     it.nmax = max(it.nA, it.nB);
     return it;
 }
@@ -99,9 +111,10 @@ __device__ __forceinline__ int item_index(int r, int c, int G) {
 }
 
 // The first item after the r-th of CTA c that has a key tile (nmax = 0 if none is left).
-__device__ __forceinline__ Item next_item(const Args &a, int r, int c, int G, int total) {
+template <bool kShard>
+__device__ __forceinline__ Item next_item(const Args &a, const DropArgs &dr, int r, int c, int G, int total) {
     for (int k = item_index(++r, c, G); k < total; k = item_index(++r, c, G)) {
-        const Item it = decode_item(a, k, false);
+        const Item it = decode_item<kShard>(a, dr, k, false);
         if (it.nmax > 0) return it;
     }
     Item none{};
@@ -121,7 +134,10 @@ __device__ __forceinline__ uint4 ld_keep(const uint8_t *p) {
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
-template <int DK, int DV, bool kBias, bool kDrop>
+// kPartial: write each row's state (m, l, u) over the kernel's keys to dr.part ([B, H, Nq,
+// 2 + DV] fp32; m the row's reference in natural-log units, l and u measured against it;
+// (-inf, 0, 0) for a row that sees no key) instead of o and lse.
+template <int DK, int DV, bool kBias, bool kDrop, bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -169,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tm_o);
         // this thread is the producer: the first item's Q_A and K_0 start loading before the
         // tensor-memory allocation and the block barrier
-        const Item it = next_item(a, -1, cta, G, total);
+        const Item it = next_item<kPartial>(a, dr, -1, cta, G, total);
         if (it.nmax > 0) {
             if (it.nA > 0) {
                 ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], L::kQBytes);
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = 0; ok; ++r) {
                 const int k = item_index(r, cta, G);
                 if (k >= total) break;
-                const Item it = decode_item(a, k, false);
+                const Item it = decode_item<kPartial>(a, dr, k, false);
                 if (it.nmax == 0) continue;
                 // Q_A, K_0, Q_B, V_0, K_1, ...: S_A(0) needs only the first two
                 if (it.nA > 0 && !(g == 0 && pre_q) && !load_q(0, nqA, it)) break;
@@ -331,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = 0; ok; ++r) {
                 const int k = item_index(r, cta, G);
                 if (k >= total) break;
-                const Item it = decode_item(a, k, false);
+                const Item it = decode_item<kPartial>(a, dr, k, false);
                 if (it.nmax == 0) continue;
                 const int nA = it.nA, nB = it.nB, nmax = it.nmax;
                 if (nA > 0 && !first_s(0, nA, nqA, g)) break;
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rr = 0; ok; ++rr) {
             const int k = item_index(rr, cta, G);
             if (k >= total) break;
-            const Item it = decode_item(a, k, threadIdx.x == 128);
+            const Item it = decode_item<kPartial>(a, dr, k, threadIdx.x == 128);
             const int nX = X ? it.nB : it.nA;
             const int r0 = it.q0 + X * BQ, i = r0 + r;
             // this row's output and log-sum-exp (null past Nq)
@@ -386,11 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return (a.lse && i < a.Nq) ? a.lse + ((long long)it.b * a.H + it.h) * a.Nq + i : nullptr;
             };
             if (nX == 0) {  // no key visible to any row of this tile
-                if (i < a.Nq) write_empty_row<DV>(out_row(), out_lse());
+                if (i < a.Nq) {
+                    if constexpr (kPartial) write_empty_state<DV>(dr.part + (((long long)it.b * a.H + it.h) * a.Nq + i) * (2 + DV));
+                    else write_empty_row<DV>(out_row(), out_lse());
+                }
                 g += it.nmax;
                 continue;
             }
-            const int shift = it.n - a.Nq;
+            const int shift = it.shift;
             const float *bias_row = nullptr;
             if (kBias && i < a.Nq) bias_row = a.bias + it.b * a.bs0 + it.h * a.bs1 + (long long)i * a.bs2;
             const bool bias_vec = (reinterpret_cast<uintptr_t>(bias_row) & 15u) == 0;
@@ -445,6 +464,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok || !wait_warp(&ctrl->o_final[X], nfin & 1)) break;
             ptx::tc_fence_after();
+            if constexpr (kPartial) {
+                // the row's state goes straight to global memory; the buffers the staged store
+                // would have released are released here
+                write_state<DV>(lane_addr + o_col, l_run, m_run,
+                                i < a.Nq ? dr.part + (((long long)it.b * a.H + it.h) * a.Nq + i) * (2 + DV)
+                                         : nullptr);
+                ptx::tc_fence_before();
+                if (r == 0) {
+                    if (X) ptx::mbar_arrive(&ctrl->v_empty[(g + it.nmax - 1) % VS]);
+                    else if (kStageA) ptx::mbar_arrive(&ctrl->q_empty[0]);
+                }
+                g += it.nmax;
+                u += nX;
+                ++nfin;
+                continue;
+            }
             // divide once and store the row; the next item's first P V product overwrites O_X
             // only after this thread's next P hand-off, which follows these TMEM loads
             // Each tile's rows go through shared memory in the swizzled box layout, and one
@@ -491,11 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int DK, int DV, bool kBias, bool kDrop>
+template <int DK, int DV, bool kBias, bool kDrop, bool kPartial = false>
 attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                        const CUtensorMap &mo, const Args &a, const DropArgs &dr, cudaStream_t s) {
     const int smem = Layout<DK, DV>::kBytes;
-    auto kern = fwd_bf16_pair_kernel<DK, DV, kBias, kDrop>;
+    auto kern = fwd_bf16_pair_kernel<DK, DV, kBias, kDrop, kPartial>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const long long total = (long long)a.n_items * a.B * a.H;
@@ -516,6 +551,15 @@ attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
                                    const CUtensorMap &mv, const CUtensorMap &mo,
                                    const bf16fwd::Args &a, const bf16fwd::DropArgs &dr, int dk, int dv, bool bias,
                                    cudaStream_t s) {
+    if (dr.part) {  // partial states: dk == dv in {64, 128}, no dropout (checked by the caller)
+        if (dk == 128 && dv == 128)
+            return bias ? launch_t<128, 128, true, false, true>(mq, mk, mv, mo, a, dr, s)
+                        : launch_t<128, 128, false, false, true>(mq, mk, mv, mo, a, dr, s);
+        if (dk == 64 && dv == 64)
+            return bias ? launch_t<64, 64, true, false, true>(mq, mk, mv, mo, a, dr, s)
+                        : launch_t<64, 64, false, false, true>(mq, mk, mv, mo, a, dr, s);
+        return fail(ATTN_ERR_UNSUPPORTED, "partial states need dk == dv in {64, 128} (dk=%d dv=%d)", dk, dv);
+    }
 #define ATTN_PAIR_CASE(DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_) {                                                              \
         if (dr.dmask)                                                                          \

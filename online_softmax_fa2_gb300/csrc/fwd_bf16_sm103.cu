@@ -559,10 +559,13 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     a.lse = p.lse;
     a.bias = p.bias; a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1]; a.bs2 = p.bias_stride[2];
     a.kv_lens = p.kv_lens;
-    DropArgs dr;
+    DropArgs dr{};
     dr.dmask = p.dropout_mask;
     dr.dms0 = p.dropout_mask_stride[0]; dr.dms1 = p.dropout_mask_stride[1]; dr.dms2 = p.dropout_mask_stride[2];
     dr.inv_keep = p.dropout_mask ? (float)(1.0 / (1.0 - (double)p.dropout_p)) : 1.f;
+    dr.key_off = 0;
+    dr.Nk_tot = (int)p.Nk;
+    dr.part = nullptr;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     CUtensorMap mo;
@@ -576,6 +579,43 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
         return dispatch<true, true>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
     if (p.bias) return dispatch<true, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
     return dispatch<false, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
+}
+
+attn_status_t launch_fwd_bf16_partial(const attn_fwd_params_t &p, int64_t key_offset, int64_t Nk_total,
+                                      float *partials, cudaStream_t s) {
+    for (int t = 0; t < 3; ++t) {
+        if ((p.q_stride[t] == 0 && (t == 0 ? p.B : t == 1 ? p.Nq : p.H) > 1) ||
+            (p.Nk > 0 && ((p.k_stride[t] == 0 || p.v_stride[t] == 0) && (t == 0 ? p.B : t == 1 ? p.Nk : p.H) > 1)))
+            return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path needs non-zero q/k/v strides");
+    }
+    CUtensorMap mq, mk, mv;
+    attn_status_t st = encode(&mq, p.q, p.B, p.Nq, p.H, p.dk, p.q_stride, "q");
+    if (st) return st;
+    if (p.Nk > 0) {
+        if ((st = encode(&mk, p.k, p.B, p.Nk, p.H, p.dk, p.k_stride, "k"))) return st;
+        if ((st = encode(&mv, p.v, p.B, p.Nk, p.H, p.dv, p.v_stride, "v"))) return st;
+    } else {
+        mk = mq;  // never read: with no keys every tile is empty
+        mv = mq;
+    }
+    Args a;
+    a.B = (int)p.B; a.H = (int)p.H; a.Nq = (int)p.Nq; a.Nk = (int)p.Nk; a.causal = p.causal;
+    a.n_items = (int)((p.Nq + 2 * BQ - 1) / (2 * BQ));
+    a.scale_log2 = p.scale * kLog2e;
+    a.o = nullptr;
+    a.os0 = a.os1 = a.os2 = 0;
+    a.lse = nullptr;
+    a.bias = p.bias; a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1]; a.bs2 = p.bias_stride[2];
+    a.kv_lens = p.kv_lens;
+    DropArgs dr{};
+    dr.inv_keep = 1.f;
+    dr.key_off = (int)key_offset;
+    dr.Nk_tot = (int)Nk_total;
+    dr.part = partials;
+    a.flags = device_flags();
+    if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
+    // the output map is never used by the partial-state kernel
+    return launch_fwd_bf16_pair(mq, mk, mv, mq, a, dr, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
 }
 
 }  // namespace attn
