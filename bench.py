@@ -710,6 +710,7 @@ CASES = {
     # name: (workload factory kwargs, kind)
     "prefill": ("causal_2k", {}, "fwd"),
     "prefill_dropout": ("causal_2k", {}, "fwd_dropout"),
+    "prefill_dropout_rng": ("causal_2k", {}, "fwd_dropout_rng"),
     "padbias": ("padded_bias", {}, "fwd"),
     "long_causal": ("long_causal", {}, "fwd"),
     "fp32": ("fp32_small", {}, "fwd"),
@@ -721,6 +722,7 @@ CASES = {
     "decode_nq4_b16": ("decode", {"B": 16, "nq": 4, "causal": True}, "decode"),
     "bwd": ("causal_2k", {}, "bwd"),
     "bwd_dropout": ("causal_2k", {}, "bwd_dropout"),
+    "bwd_dropout_rng": ("causal_2k", {}, "bwd_dropout_rng"),
     "bwd_long": ("long_causal", {"H": 8}, "bwd"),
 }
 
@@ -736,23 +738,28 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     a = getattr(wl, fac)(dev, **kw)
     ofa.load()
-    if kind in ("fwd", "fwd_dropout"):
+    if kind in ("fwd", "fwd_dropout", "fwd_dropout_rng"):
         o = torch.empty((a.B, a.Nq, a.H, a.dv), dtype=a.q.dtype, device=dev)
         lse = torch.empty((a.B, a.H, a.Nq), dtype=torch.float32, device=dev)
-        mask, p_drop = None, 0.0
+        mask, p_drop, seed = None, 0.0, None
         if kind == "fwd_dropout":  # a seeded keep mask with p = 0.1, bit-packed (33.5 MB here)
             p_drop = 0.1
             mask = wl.pack_keep_mask(wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p_drop, seed=1, device=dev))
+        if kind == "fwd_dropout_rng":  # p = 0.1, the keep decisions drawn in-kernel
+            p_drop, seed = 0.1, 1
         fn = lambda: ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
-                                  scale=a.scale, out=o, lse=lse, dropout_mask=mask, dropout_p=p_drop)
+                                  scale=a.scale, out=o, lse=lse, dropout_mask=mask, dropout_p=p_drop,
+                                  dropout_seed=seed)
         work, unit = a.flops() / 1e12, "TFLOP/s"
-    elif kind in ("bwd", "bwd_dropout"):
-        mask, p_drop = None, 0.0
+    elif kind in ("bwd", "bwd_dropout", "bwd_dropout_rng"):
+        mask, p_drop, seed = None, 0.0, None
         if kind == "bwd_dropout":  # the forward's seeded keep mask with p = 0.1
             p_drop = 0.1
             mask = wl.pack_keep_mask(wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p_drop, seed=1, device=dev))
+        if kind == "bwd_dropout_rng":  # p = 0.1, the keep decisions drawn in-kernel
+            p_drop, seed = 0.1, 1
         o, lse = ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=a.causal,
-                              scale=a.scale, dropout_mask=mask, dropout_p=p_drop)
+                              scale=a.scale, dropout_mask=mask, dropout_p=p_drop, dropout_seed=seed)
         gen = torch.Generator(device=dev)
         gen.manual_seed(7)
         dout = torch.randn(o.shape, generator=gen, device=dev).to(o.dtype)
@@ -761,7 +768,7 @@ def run_case(args):
         dq, dk, dv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
         fn = lambda: ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, bias=a.bias, kv_lens=a.kv_lens,
                                   causal=a.causal, scale=a.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                                  dropout_mask=mask, dropout_p=p_drop)
+                                  dropout_mask=mask, dropout_p=p_drop, dropout_seed=seed)
         # 2 (S) + 2 (dP) + 2 (dV) + 2 (dK) + 2 (dQ) products: (6 dk + 4 dv) FLOPs per visible pair
         work, unit = a.visible_pairs() * (6 * a.dk + 4 * a.dv) / 1e12, "TFLOP/s"
     elif kind == "decode_fused":

@@ -111,7 +111,22 @@ typedef enum {
  *                       are multiples of 16 bytes.  Not taken by attn_decode_splitkv, nor by
  *                       attn_bwd other than for dk = dv = 128 without a bias
  *                       (ATTN_ERR_UNSUPPORTED).
- *   dropout_p           in [0, 1) with a mask; must be 0 without one.
+ *   dropout_p           in [0, 1) with a mask or with dropout_rng = 1; must be 0 otherwise.
+ *   dropout_rng         0: the keep decisions come from dropout_mask (or there is no dropout).
+ *                       1: they are drawn in-kernel, and no mask is read or stored anywhere:
+ *                       the drop probability is quantised to p8 / 256, p8 = round(256 p) (at
+ *                       most 255), and key j of row i of (b, h) is kept iff byte j % 16 of the
+ *                       counter-based generator Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
+ *                       "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) at counter
+ *                       (i, j / 16, b*H + h, dropout_offset mod 2^32) under key (dropout_seed
+ *                       mod 2^32, dropout_seed div 2^32) -- its four output words in order,
+ *                       each little-endian -- is at least p8; kept weights are scaled by
+ *                       256 / (256 - p8).  dropout_mask must then be NULL.  attn_bwd given the
+ *                       forward's (dropout_p, dropout_rng, dropout_seed, dropout_offset) draws
+ *                       the same decisions.  Where a mask is not taken (see dropout_mask), the
+ *                       in-kernel draw is not either.
+ *   dropout_seed, dropout_offset  the generator's key and the fourth counter word (a fresh
+ *                       offset per training step gives fresh decisions).
  */
 typedef struct {
     int32_t dtype;           /* attn_dtype_t */
@@ -134,6 +149,9 @@ typedef struct {
     const uint8_t *dropout_mask;
     int64_t dropout_mask_stride[3];  /* b, h, i (bytes) */
     float dropout_p;
+    int32_t dropout_rng;             /* 0: keep bits from dropout_mask; 1: drawn in-kernel */
+    uint64_t dropout_seed;
+    uint64_t dropout_offset;
 } attn_fwd_params_t;
 
 /*

@@ -68,7 +68,8 @@ class Params(ctypes.Structure):
         ("kv_lens", ctypes.c_void_p),
         ("scale", ctypes.c_float), ("block_k", ctypes.c_int32),
         ("dropout_mask", ctypes.c_void_p), ("dropout_mask_stride", ctypes.c_int64 * 3),
-        ("dropout_p", ctypes.c_float),
+        ("dropout_p", ctypes.c_float), ("dropout_rng", ctypes.c_int32),
+        ("dropout_seed", ctypes.c_uint64), ("dropout_offset", ctypes.c_uint64),
     ]
 
 
@@ -176,7 +177,7 @@ def _require_cuda(*ts):
 
 
 def make_params(q, k, v, o, lse=None, bias=None, kv_lens=None, causal=False, scale=None,
-                block_k=0, dropout_mask=None, dropout_p=0.0) -> Params:
+                block_k=0, dropout_mask=None, dropout_p=0.0, dropout_seed=None, dropout_offset=0) -> Params:
     """Fill an attn_fwd_params_t from tensors (no computation)."""
     _require_cuda(q, k, v, o, lse, bias, kv_lens, dropout_mask)
     B, Nq, H, dk = q.shape
@@ -224,15 +225,21 @@ def make_params(q, k, v, o, lse=None, bias=None, kv_lens=None, causal=False, sca
         p.dropout_mask = mm.data_ptr()
         p.dropout_mask_stride = (ctypes.c_int64 * 3)(mm.stride(0), mm.stride(1), mm.stride(2))
     p.dropout_p = float(dropout_p)
+    if dropout_seed is not None:  # keep decisions drawn in-kernel (Philox4x32-10; see attn.h)
+        p.dropout_rng = 1
+        p.dropout_seed = int(dropout_seed) & 0xFFFFFFFFFFFFFFFF
+        p.dropout_offset = int(dropout_offset) & 0xFFFFFFFFFFFFFFFF
     return p
 
 
 def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, block_k=0, out=None,
-             lse=None, stream=None, dropout_mask=None, dropout_p=0.0):
+             lse=None, stream=None, dropout_mask=None, dropout_p=0.0, dropout_seed=None, dropout_offset=0):
     """Exact attention forward; returns (o, lse).  See include/attn.h, attn_fwd.  With a
     dropout_mask (uint8 [B, H, Nq, 16 * ceil(Nk / 128)], workloads.pack_keep_mask) the kept
     weights are scaled by 1 / (1 - dropout_p) and the dropped ones count 0 in o; lse is the
-    undropped one."""
+    undropped one.  With dropout_seed (and dropout_offset) instead of a mask the keep
+    decisions are drawn in-kernel (Philox4x32-10, p quantised to round(256 p) / 256); the
+    backward given the same seed and offset draws the same ones."""
     lib = load()
     B, Nq, H, _ = q.shape
     dv = v.shape[3]
@@ -240,7 +247,8 @@ def attn_fwd(q, k, v, bias=None, kv_lens=None, causal=False, scale=None, block_k
         out = torch.empty((B, Nq, H, dv), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, block_k, dropout_mask, dropout_p)
+    p = make_params(q, k, v, out, lse, bias, kv_lens, causal, scale, block_k, dropout_mask, dropout_p,
+                    dropout_seed, dropout_offset)
     _check(lib.attn_fwd(ctypes.byref(p), _stream(stream)))
     return out, lse
 
@@ -367,7 +375,8 @@ def bwd_workspace_bytes(B, H, Nq, dk) -> int:
 
 
 def attn_bwd(q, k, v, o, lse, dout, bias=None, kv_lens=None, causal=False, scale=None,
-             dq=None, dk=None, dv=None, workspace=None, stream=None, dropout_mask=None, dropout_p=0.0):
+             dq=None, dk=None, dv=None, workspace=None, stream=None, dropout_mask=None, dropout_p=0.0,
+             dropout_seed=None, dropout_offset=0):
     """Gradients (dq, dk, dv) of a loss through o = attn_fwd(q, k, v, ...), given dout = dL/do
     and the forward's o and lse (bfloat16, dk == dv in {64, 128}).  The mask, bias, kv_lens,
     causal and dropout settings must be the forward's (dropout: dk = dv = 128 without a bias);
@@ -385,7 +394,8 @@ def attn_bwd(q, k, v, o, lse, dout, bias=None, kv_lens=None, causal=False, scale
         workspace = torch.empty((max(need, 16) + 3) // 4, dtype=torch.float32, device=q.device)
     _require_cuda(dout, dq, dk, dv, workspace)
     p = BwdParams()
-    p.fwd = make_params(q, k, v, o, lse, bias, kv_lens, causal, scale, 0, dropout_mask, dropout_p)
+    p.fwd = make_params(q, k, v, o, lse, bias, kv_lens, causal, scale, 0, dropout_mask, dropout_p, dropout_seed,
+                        dropout_offset)
     p.dout, p.dout_stride = dout.data_ptr(), _bnhd_strides(dout, "dout")
     p.dq, p.dq_stride = dq.data_ptr(), _bnhd_strides(dq, "dq")
     p.dk, p.dk_stride = dk.data_ptr(), _bnhd_strides(dk, "dk")

@@ -64,6 +64,9 @@ static attn_status_t check_strides(const char *name, const int64_t s[3]) {
     return ATTN_OK;
 }
 
+// Dropout of a training forward: a keep mask given, or the keep decisions drawn in-kernel.
+static bool has_dropout(const attn_fwd_params_t *p) { return p->dropout_mask || p->dropout_rng == 1; }
+
 // Checks shared by attn_fwd and attn_decode_splitkv.
 static attn_status_t check_common(const attn_fwd_params_t *p) {
     if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
@@ -89,12 +92,16 @@ static attn_status_t check_common(const attn_fwd_params_t *p) {
         for (int i = 0; i < 3; ++i)
             if (p->bias_stride[i] < 0)
                 return fail(ATTN_ERR_INVALID_ARG, "bias_stride[%d] is negative", i);
-    if (p->dropout_mask) {
+    if (p->dropout_rng != 0 && p->dropout_rng != 1)
+        return fail(ATTN_ERR_INVALID_ARG, "dropout_rng must be 0 or 1 (got %d)", p->dropout_rng);
+    if (p->dropout_rng == 1 && p->dropout_mask)
+        return fail(ATTN_ERR_INVALID_ARG, "dropout_rng = 1 draws the keep decisions: dropout_mask must be NULL");
+    if (has_dropout(p)) {
         if (!(p->dropout_p >= 0.0f && p->dropout_p < 1.0f))
             return fail(ATTN_ERR_INVALID_ARG, "dropout_p must be in [0, 1) (got %g)", p->dropout_p);
-        if ((st = check_strides("dropout_mask", p->dropout_mask_stride))) return st;
+        if (p->dropout_mask && (st = check_strides("dropout_mask", p->dropout_mask_stride))) return st;
     } else if (p->dropout_p != 0.0f) {
-        return fail(ATTN_ERR_INVALID_ARG, "dropout_p = %g without a dropout_mask", p->dropout_p);
+        return fail(ATTN_ERR_INVALID_ARG, "dropout_p = %g without a dropout_mask or dropout_rng", p->dropout_p);
     }
     if (p->B * p->H * p->Nq == 0) return ATTN_OK;
     if (!p->q || !p->o) return fail(ATTN_ERR_INVALID_ARG, "q or o is NULL");
@@ -144,9 +151,9 @@ extern "C" attn_status_t attn_fwd(const attn_fwd_params_t *p, attn_stream_t stre
         return fail(ATTN_ERR_MISALIGNED, "bfloat16 strides must be multiples of 8 elements");
     if (p->bias && (reinterpret_cast<uintptr_t>(p->bias) & 3u))
         return fail(ATTN_ERR_MISALIGNED, "bias must be 4-byte aligned");
-    if (p->dropout_mask) {
+    if (has_dropout(p)) {
         if (p->dk > 128) return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 dropout supports dk <= 128");
-        if (!aligned16(p->dropout_mask) || !stride_mult(p->dropout_mask_stride, 16))
+        if (p->dropout_mask && (!aligned16(p->dropout_mask) || !stride_mult(p->dropout_mask_stride, 16)))
             return fail(ATTN_ERR_MISALIGNED, "dropout_mask must be 16-byte aligned with strides that are multiples of 16 bytes");
     }
     return launch_fwd_bf16(*p, s);
@@ -177,7 +184,7 @@ attn_status_t check_decode_args(const attn_fwd_params_t *p, int32_t num_splits) 
         return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in [1, 256] (got %d)", num_splits);
     if (p->dtype != ATTN_DTYPE_BF16)
         return fail(ATTN_ERR_UNSUPPORTED, "decode supports bfloat16 only");
-    if (p->dropout_mask) return fail(ATTN_ERR_UNSUPPORTED, "decode takes no dropout mask");
+    if (has_dropout(p)) return fail(ATTN_ERR_UNSUPPORTED, "decode takes no dropout");
     if (p->dk != p->dv || (p->dk != 64 && p->dk != 128))
         return fail(ATTN_ERR_UNSUPPORTED, "decode supports dk == dv in {64, 128} (dk=%lld dv=%lld)",
                     (long long)p->dk, (long long)p->dv);
@@ -267,7 +274,7 @@ extern "C" attn_status_t attn_fwd_partial(const attn_fwd_params_t *p, int64_t ke
     if (p->dk != p->dv || (p->dk != 64 && p->dk != 128))
         return fail(ATTN_ERR_UNSUPPORTED, "partial states support dk == dv in {64, 128} (dk=%lld dv=%lld)",
                     (long long)p->dk, (long long)p->dv);
-    if (p->dropout_mask) return fail(ATTN_ERR_UNSUPPORTED, "partial states take no dropout mask");
+    if (has_dropout(p)) return fail(ATTN_ERR_UNSUPPORTED, "partial states take no dropout");
     if (p->block_k != 0) return fail(ATTN_ERR_INVALID_ARG, "block_k must be 0 for bfloat16 (got %d)", p->block_k);
     if (!(p->scale > 0.0f)) return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 path needs scale > 0 (got %g)", p->scale);
     if (key_offset < 0 || Nk_total < key_offset + p->Nk || Nk_total > INT32_MAX)
@@ -334,10 +341,10 @@ extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, s
     attn_status_t st = check_common(f);
     if (st) return st;
     if (f->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward supports bfloat16 only");
-    if (f->dropout_mask) {  // the backward of a dropout forward runs on the d = 128 tcgen05 kernel
+    if (has_dropout(f)) {  // the backward of a dropout forward runs on the d = 128 tcgen05 kernel
         if (f->dk != 128 || f->dv != 128 || f->bias)
             return fail(ATTN_ERR_UNSUPPORTED, "the backward of a dropout forward supports dk = dv = 128 without a bias");
-        if (!aligned16(f->dropout_mask) || !stride_mult(f->dropout_mask_stride, 16))
+        if (f->dropout_mask && (!aligned16(f->dropout_mask) || !stride_mult(f->dropout_mask_stride, 16)))
             return fail(ATTN_ERR_MISALIGNED, "dropout_mask must be 16-byte aligned with strides that are multiples of 16 bytes");
     }
     if (f->dk != f->dv || (f->dk != 64 && f->dk != 128))

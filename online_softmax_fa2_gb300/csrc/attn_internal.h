@@ -58,4 +58,12 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// In-kernel dropout draws (dropout_rng = 1): the drop probability quantised to p8 / 256 with
+// p8 = round(256 p), at most 255 (see include/attn.h).
+inline uint32_t dropout_p8(float p) {
+    const double x = (double)p * 256.0 + 0.5;
+    const uint32_t q = x <= 0.0 ? 0u : (uint32_t)x;
+    return q > 255u ? 255u : q;
+}
+
 }  // namespace attn

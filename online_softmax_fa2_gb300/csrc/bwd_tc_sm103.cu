@@ -370,14 +370,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int it = i0 + 32 * c + lane;
                 Cq[c] = it < a.Nq ? __ldg(c_bh + it) : 0.f;
             }
-            // dropout: lane t holds, for rows 32c + t, the keep bits of this warp's 32 keys
+            // dropout: lane t holds, for rows 32c + t, the keep bits of this warp's 32 keys (from
+            // the forward's mask, or drawn in-kernel as the forward drew them)
             uint32_t Zq[4];
             if constexpr (kDrop) {
-                const uint8_t *zb = dr.dmask + b * dr.dms0 + h * dr.dms1 + (j0 + 32 * (warp & 3)) / 8;
+                const int jw = j0 + 32 * (warp & 3);
+                if (dr.rng) {
+                    // row it sees keys < vis (its sequence's keys, and under the causal mask
+                    // keys <= it + shift): groups of 16 keys past them are not drawn
+                    const uint32_t bh = (uint32_t)(b * a.H + h), g0 = (uint32_t)(jw >> 4);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int it = i0 + 32 * c + lane;
-                    Zq[c] = it < a.Nq ? __ldg(reinterpret_cast<const uint32_t *>(zb + (long long)it * dr.dms2)) : 0u;
+                    for (int c = 0; c < 4; ++c) {
+                        const int it = i0 + 32 * c + lane;
+                        const int vis = (a.causal ? min(n, it + shift + 1) : n) - jw;
+                        uint32_t z = 0u;
+                        if (it < a.Nq && vis > 0) {
+                            z = rng::keep16((uint32_t)it, g0, bh, dr.offset, dr.seed_lo, dr.seed_hi, dr.p8x4);
+                            if (vis > 16)
+                                z |= rng::keep16((uint32_t)it, g0 + 1, bh, dr.offset, dr.seed_lo, dr.seed_hi, dr.p8x4)
+                                     << 16;
+                        }
+                        Zq[c] = z;
+                    }
+                } else {
+                    const uint8_t *zb = dr.dmask + b * dr.dms0 + h * dr.dms1 + jw / 8;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int it = i0 + 32 * c + lane;
+                        Zq[c] = it < a.Nq ? __ldg(reinterpret_cast<const uint32_t *>(zb + (long long)it * dr.dms2)) : 0u;
+                    }
                 }
             }
             for (int hh = 0; ok && hh < 2; ++hh) {
@@ -563,11 +584,9 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     a.dvs0 = p.dv_stride[0]; a.dvs1 = p.dv_stride[1]; a.dvs2 = p.dv_stride[2];
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
-    bf16fwd::DropArgs dr;
-    dr.dmask = f.dropout_mask;
-    dr.dms0 = f.dropout_mask_stride[0]; dr.dms1 = f.dropout_mask_stride[1]; dr.dms2 = f.dropout_mask_stride[2];
-    dr.inv_keep = f.dropout_mask ? (float)(1.0 / (1.0 - (double)f.dropout_p)) : 1.f;
-    auto kernel = f.dropout_mask ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
+    bf16fwd::DropArgs dr{};
+    fill_dropout(dr, f);
+    auto kernel = (dr.dmask || dr.rng) ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     if ((f.Nk + BK - 1) / BK > 65535 || f.B > 65535)

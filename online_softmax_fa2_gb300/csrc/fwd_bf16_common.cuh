@@ -9,6 +9,7 @@
 #include <cmath>
 
 #include "attn_internal.h"
+#include "dropout_rng.cuh"
 #include "sm100_ptx.cuh"
 
 namespace attn {
@@ -46,10 +47,30 @@ struct Args {
 struct DropArgs {
     const uint8_t *dmask;
     long long dms0, dms1, dms2;
-    float inv_keep;  // 1 / (1 - dropout_p)
+    float inv_keep;  // 1 / (1 - dropout_p), the realised p for in-kernel draws
     int key_off, Nk_tot;
     float *part;
+    // in-kernel draws (rng != 0): Philox4x32-10 under key (seed_lo, seed_hi), fourth counter
+    // word offset, byte threshold p8 in each byte of p8x4 (dropout_rng.cuh)
+    int rng;
+    uint32_t seed_lo, seed_hi, offset, p8x4;
 };
+
+// The DropArgs fields of a forward's dropout settings (mask or in-kernel draws).
+inline void fill_dropout(DropArgs &dr, const attn_fwd_params_t &p) {
+    dr.dmask = p.dropout_mask;
+    dr.dms0 = p.dropout_mask_stride[0];
+    dr.dms1 = p.dropout_mask_stride[1];
+    dr.dms2 = p.dropout_mask_stride[2];
+    dr.rng = p.dropout_rng == 1;
+    const uint32_t p8 = dropout_p8(p.dropout_p);
+    dr.seed_lo = (uint32_t)(p.dropout_seed & 0xffffffffu);
+    dr.seed_hi = (uint32_t)(p.dropout_seed >> 32);
+    dr.offset = (uint32_t)(p.dropout_offset & 0xffffffffu);
+    dr.p8x4 = p8 * 0x01010101u;
+    dr.inv_keep = dr.rng ? (float)(256.0 / (256.0 - (double)p8))
+                         : p.dropout_mask ? (float)(1.0 / (1.0 - (double)p.dropout_p)) : 1.f;
+}
 
 // Key length of sequence b, clamped to [0, Nk] (a clamp is reported once per sequence); Nk is
 // the whole sequence's key count (a.Nk unless the kernel computes over one shard).

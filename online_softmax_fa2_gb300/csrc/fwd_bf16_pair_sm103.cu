@@ -418,12 +418,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x[BK];  // with a bias: the next tile's bias, loaded ahead
             if (kBias) load_bias(bias_row, bias_vec, 0, it.n, x);
             // dropout: this row's keep bits, 16 bytes per key tile, the next tile's loaded ahead
+            // from the mask, or drawn in-kernel while the thread waits for the next S
             const uint8_t *keep_row = nullptr;
             uint4 keep = make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t bh = (uint32_t)(it.b * a.H + it.h);
             if constexpr (kDrop) {
                 if (i < a.Nq) {
-                    keep_row = dr.dmask + it.b * dr.dms0 + it.h * dr.dms1 + (long long)i * dr.dms2;
-                    keep = ld_keep(keep_row);
+                    if (dr.rng) {
+                        keep = rng::keep128((uint32_t)i, 0u, bh, dr.offset, dr.seed_lo, dr.seed_hi, dr.p8x4);
+                    } else {
+                        keep_row = dr.dmask + it.b * dr.dms0 + it.h * dr.dms1 + (long long)i * dr.dms2;
+                        keep = ld_keep(keep_row);
+                    }
                 }
             }
             for (int j = 0; j < nX; ++j) {
@@ -461,6 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&ctrl->p_full[X]);
                 if (kBias && j + 1 < nX) load_bias(bias_row, bias_vec, kv0 + BK, it.n, x);
+                if constexpr (kDrop) {
+                    if (dr.rng && i < a.Nq && j + 1 < nX)
+                        keep = rng::keep128((uint32_t)i, (uint32_t)(kv0 + BK), bh, dr.offset, dr.seed_lo, dr.seed_hi,
+                                            dr.p8x4);
+                }
             }
             if (!ok || !wait_warp(&ctrl->o_final[X], nfin & 1)) break;
             ptx::tc_fence_after();
@@ -562,7 +573,7 @@ attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
     }
 #define ATTN_PAIR_CASE(DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_) {                                                              \
-        if (dr.dmask)                                                                          \
+        if (dr.dmask || dr.rng)                                                                \
             return bias ? launch_t<DK_, DV_, true, true>(mq, mk, mv, mo, a, dr, s)                 \
                         : launch_t<DK_, DV_, false, true>(mq, mk, mv, mo, a, dr, s);               \
         return bias ? launch_t<DK_, DV_, true, false>(mq, mk, mv, mo, a, dr, s)                    \

@@ -560,9 +560,7 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     a.bias = p.bias; a.bs0 = p.bias_stride[0]; a.bs1 = p.bias_stride[1]; a.bs2 = p.bias_stride[2];
     a.kv_lens = p.kv_lens;
     DropArgs dr{};
-    dr.dmask = p.dropout_mask;
-    dr.dms0 = p.dropout_mask_stride[0]; dr.dms1 = p.dropout_mask_stride[1]; dr.dms2 = p.dropout_mask_stride[2];
-    dr.inv_keep = p.dropout_mask ? (float)(1.0 / (1.0 - (double)p.dropout_p)) : 1.f;
+    fill_dropout(dr, p);
     dr.key_off = 0;
     dr.Nk_tot = (int)p.Nk;
     dr.part = nullptr;
@@ -571,7 +569,7 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     CUtensorMap mo;
     if ((st = encode(&mo, p.o, p.B, p.Nq, p.H, p.dv, p.o_stride, "o"))) return st;
     if (pair) return launch_fwd_bf16_pair(mq, mk, mv, mo, a, dr, (int)p.dk, (int)p.dv, p.bias != nullptr, s);
-    if (dr.dmask) return fail(ATTN_ERR_UNSUPPORTED, "dropout with dk = %lld is not built", (long long)p.dk);
+    if (dr.dmask || dr.rng) return fail(ATTN_ERR_UNSUPPORTED, "dropout with dk = %lld is not built", (long long)p.dk);
     const long long grid = (long long)a.n_items * p.B * p.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
     CUtensorMap mb = mq;  // read only by kernels that stage the bias

@@ -16,6 +16,7 @@
 #include <cmath>
 
 #include "attn_internal.h"
+#include "dropout_rng.cuh"
 
 namespace attn {
 namespace {
@@ -37,7 +38,9 @@ struct F32Args {
     uint32_t *flags;
     const uint8_t *dmask;  // dropout keep bits (bit j % 8 of byte j / 8 of a row), or null
     long long dms0, dms1, dms2;
-    float inv_keep;        // 1 / (1 - dropout_p)
+    float inv_keep;        // 1 / (1 - dropout_p), the realised p for in-kernel draws
+    int rng;               // keep decisions drawn in-kernel (dropout_rng.cuh)
+    uint32_t seed_lo, seed_hi, offset, p8x4;
 };
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -153,6 +156,11 @@ __global__ void __launch_bounds__(kThreads) fwd_f32_kernel(F32Args a) {
                     const int j = j0 + jj;
                     const uint8_t bits = a.dmask[b * a.dms0 + h * a.dms1 + (long long)i * a.dms2 + (j >> 3)];
                     p = ((bits >> (j & 7)) & 1u) ? p * a.inv_keep : 0.f;
+                } else if (a.rng && vis[u]) {  // the same, drawn in-kernel (one draw per 16 keys)
+                    const int j = j0 + jj;
+                    const uint32_t bits = rng::keep16((uint32_t)i, (uint32_t)(j >> 4), (uint32_t)(b * a.H + h), a.offset,
+                                                      a.seed_lo, a.seed_hi, a.p8x4);
+                    p = ((bits >> (j & 15)) & 1u) ? p * a.inv_keep : 0.f;
                 }
                 if (jj < BK) Ps[warp * BK + jj] = p;
             }
@@ -221,7 +229,14 @@ attn_status_t launch_fwd_f32(const attn_fwd_params_t &p, cudaStream_t s) {
     a.kv_lens = p.kv_lens;
     a.dmask = p.dropout_mask;
     a.dms0 = p.dropout_mask_stride[0]; a.dms1 = p.dropout_mask_stride[1]; a.dms2 = p.dropout_mask_stride[2];
-    a.inv_keep = p.dropout_mask ? (float)(1.0 / (1.0 - (double)p.dropout_p)) : 1.f;
+    a.rng = p.dropout_rng == 1;
+    const uint32_t p8 = dropout_p8(p.dropout_p);
+    a.seed_lo = (uint32_t)(p.dropout_seed & 0xffffffffu);
+    a.seed_hi = (uint32_t)(p.dropout_seed >> 32);
+    a.offset = (uint32_t)(p.dropout_offset & 0xffffffffu);
+    a.p8x4 = p8 * 0x01010101u;
+    a.inv_keep = a.rng ? (float)(256.0 / (256.0 - (double)p8))
+                       : p.dropout_mask ? (float)(1.0 / (1.0 - (double)p.dropout_p)) : 1.f;
     a.flags = device_flags();
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     if (p.B > 65535 || p.H > 65535)

@@ -151,3 +151,92 @@ def test_bwd_dropout_full_size_one_head():
     ct = dq_c_term(sl(dout), sl(run_bwd_drop.last_o), sl(a.k), a.scale)
     for got, ref, name in zip(grads, refs, ("dq", "dk", "dv")):
         check_grad(got[b:b + 1, :, h:h + 1], ref, f"{name} full-size head", extra=ct if name == "dq" else None)
+
+
+# ---------------------------------------------------------------- keep decisions drawn in-kernel
+# (Philox4x32-10, include/attn.h dropout_rng).  The oracle restates the generator
+# (oracle/philox.py, pinned to the published known-answer vectors) and draws the same
+# decisions; feeding them to the kernel as a mask must give the same output bit for bit, and
+# both must match the dropout oracle.
+
+from oracle import philox as _philox  # noqa: E402
+
+
+def _rng_keep(a, seed, offset, p):
+    keep, p_real = _philox.keep_mask(seed, offset, a.B, a.H, a.Nq, a.Nk, p)
+    return torch.from_numpy(keep).to(DEV), p_real
+
+
+@pytest.mark.parametrize("dk,dv,causal,bias,p", [
+    (128, 128, True, False, 0.2),
+    (64, 64, False, True, 0.5),
+    (128, 64, True, False, 0.1),
+])
+def test_bf16_in_kernel_draws_equal_the_oracles_generator(dk, dv, causal, bias, p):
+    a = wl.make_prefill(2, 3, 300, 333, dk, dv, torch.bfloat16, causal=causal, bias=bias,
+                        kv_lens=[333, 170], seed=47, device=DEV)
+    seed, offset = 0x0123_4567_89AB_CDEF, 11
+    o1, l1 = ofa.attn_fwd(a.q, a.k, a.v, bias=a.bias, kv_lens=a.kv_lens, causal=causal, scale=a.scale,
+                          dropout_p=p, dropout_seed=seed, dropout_offset=offset)
+    keep, p_real = _rng_keep(a, seed, offset, p)
+    o2, l2 = run(a, keep, p_real)  # the same decisions, as a keep mask
+    torch.cuda.synchronize()
+    assert ofa.device_error_flags() & 1 == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+    o_ref, l_ref = ref(a, keep, p_real)
+    err = float(np.max(np.abs(o1.float().cpu().numpy() - o_ref)))
+    assert err <= TOL[torch.bfloat16]["o"] / (1.0 - p_real), err
+
+
+def test_fp32_in_kernel_draws_equal_the_oracles_generator():
+    a = wl.make_prefill(1, 2, 100, 130, 64, 64, torch.float32, causal=True, kv_lens=[130], seed=48, device=DEV)
+    seed, offset, p = 99, 3, 0.3
+    o1, l1 = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=True, scale=a.scale, dropout_p=p,
+                          dropout_seed=seed, dropout_offset=offset)
+    keep, p_real = _rng_keep(a, seed, offset, p)
+    o_ref, l_ref = ref(a, keep, p_real)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(o1.cpu().numpy() - o_ref)) <= 1e-5 / (1.0 - p_real)
+
+
+@pytest.mark.parametrize("causal,p,lens", [(True, 0.2, [333, 170]), (False, 0.5, [301, 333])])
+def test_bwd_in_kernel_draws_match_oracle(causal, p, lens):
+    a = wl.make_prefill(2, 2, 300, 333, 128, 128, torch.bfloat16, causal=causal, kv_lens=lens, seed=49,
+                        device=DEV)
+    seed, offset = 1234567, 5
+    o, lse = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=causal, scale=a.scale, dropout_p=p,
+                          dropout_seed=seed, dropout_offset=offset)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(2100)
+    dout = torch.randn(o.shape, generator=g, device=DEV).to(o.dtype)
+    grads = ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, kv_lens=a.kv_lens, causal=causal, scale=a.scale,
+                         dropout_p=p, dropout_seed=seed, dropout_offset=offset)
+    keep, p_real = _rng_keep(a, seed, offset, p)
+    # the backward with the oracle's decisions as a mask: bit for bit the same dK and dV
+    grads_m = ofa.attn_bwd(a.q, a.k, a.v, o, lse, dout, kv_lens=a.kv_lens, causal=causal, scale=a.scale,
+                           dropout_mask=wl.pack_keep_mask(keep), dropout_p=p_real)
+    torch.cuda.synchronize()
+    assert ofa.device_error_flags() & 1 == 0
+    assert torch.equal(grads[1].view(torch.int16), grads_m[1].view(torch.int16))
+    assert torch.equal(grads[2].view(torch.int16), grads_m[2].view(torch.int16))
+    refs = oracle.attn_bwd_dropout(cpu32(a.q), cpu32(a.k), cpu32(a.v), cpu32(dout), keep.cpu(), p_real,
+                                   kv_lens=a.kv_lens.cpu(), causal=causal, scale=a.scale)
+    ct = dq_c_term(dout, o, a.k, a.scale, a.kv_lens)
+    for got, r, name in zip(grads, refs, ("dq", "dk", "dv")):
+        check_grad(got, r, f"{name} in-kernel draws causal={causal} p={p}", extra=ct if name == "dq" else None)
+
+
+def test_full_size_forward_in_kernel_draws_one_head():
+    a = wl.causal_2k(DEV)
+    seed, offset, p = 77, 1, 0.1
+    o, lse = ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale, dropout_p=p, dropout_seed=seed,
+                          dropout_offset=offset)
+    torch.cuda.synchronize()
+    b, h = 1, 6
+    keep, p_real = _philox.keep_mask(seed, offset, a.B, a.H, a.Nq, a.Nk, p, heads=[(b, h)])
+    sl = lambda t: cpu32(t[b:b + 1, :, h:h + 1])
+    o_ref, l_ref = oracle.attn_fwd_dropout(sl(a.q), sl(a.k), sl(a.v), torch.from_numpy(keep)[None], p_real,
+                                           causal=True, scale=a.scale)
+    err = float(np.max(np.abs(o[b:b + 1, :, h:h + 1].float().cpu().numpy() - o_ref)))
+    assert err <= TOL[torch.bfloat16]["o"] / (1.0 - p_real), err
