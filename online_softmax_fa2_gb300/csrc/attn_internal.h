@@ -66,4 +66,25 @@ inline uint32_t dropout_p8(float p) {
     return q > 255u ? 255u : q;
 }
 
+// Launches kern as a programmatic dependent of the previous kernel in the stream: its CTAs
+// may be scheduled once every CTA of that kernel has executed griddepcontrol.launch_dependents
+// (or exited), so its launch and set-up overlap that kernel's tail.  A kernel launched this
+// way executes griddepcontrol.wait before it reads or writes global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace attn

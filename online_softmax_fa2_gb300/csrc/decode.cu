@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
+#include "sm100_ptx.cuh"
 #include "warp_mma.cuh"
 
 namespace attn {
@@ -198,6 +199,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
 
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int g = threadIdx.x / LPK, sub = threadIdx.x % LPK, c0 = sub * 8;
+    // launched as a programmatic dependent: global memory only after the previous kernel
+    ptx::grid_dep_wait();
+    ptx::launch_dependents();
 
     int n = a.Nk;
     if (a.kv_lens) {
@@ -350,6 +354,9 @@ __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nq = a.Nq;
+    // launched as a programmatic dependent: global memory only after the previous kernel
+    ptx::grid_dep_wait();
+    ptx::launch_dependents();
 
     int n = a.Nk;
     if (a.kv_lens) {
@@ -522,6 +529,8 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const float *part, long
                                                            long long rs, long long ss, int dv, OutT *o,
                                                            long long os0, long long os1, long long os2,
                                                            float *lse) {
+    ptx::grid_dep_wait();  // the partial states come from the kernel before this one
+    ptx::launch_dependents();
     const long long row = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int i = (int)(row % Nq), bh = (int)(row / Nq), b = bh / H, h = bh % H;
@@ -534,8 +543,7 @@ cudaError_t launch_rows(const DecArgs &a, dim3 grid, cudaStream_t st) {
     cudaError_t e =
         cudaFuncSetAttribute(decode_rows_mma_kernel<D, kFuse>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_rows_mma_kernel<D, kFuse><<<grid, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_rows_mma_kernel<D, kFuse>, grid, dim3(kThreads), smem, st, a);
 }
 
 }  // namespace
@@ -569,13 +577,9 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
     cudaError_t e = cudaSuccess;
     const bool fuse = counters != nullptr;
     if (p.Nq == 1) {
-        if (p.dk == 64) {
-            if (fuse) decode_split_kernel<64, true><<<grid, kThreads, 0, st>>>(a);
-            else decode_split_kernel<64, false><<<grid, kThreads, 0, st>>>(a);
-        } else {
-            if (fuse) decode_split_kernel<128, true><<<grid, kThreads, 0, st>>>(a);
-            else decode_split_kernel<128, false><<<grid, kThreads, 0, st>>>(a);
-        }
+        auto kern = p.dk == 64 ? (fuse ? decode_split_kernel<64, true> : decode_split_kernel<64, false>)
+                               : (fuse ? decode_split_kernel<128, true> : decode_split_kernel<128, false>);
+        e = launch_pdl(kern, grid, dim3(kThreads), 0, st, a);
     } else if (p.dk == 64) {
         e = fuse ? launch_rows<64, true>(a, grid, st) : launch_rows<64, false>(a, grid, st);
     } else {
@@ -595,15 +599,14 @@ attn_status_t launch_merge(const float *partials, int64_t B, int64_t H, int64_t 
     const long long ss = split_stride ? split_stride : 2 + dv;
     if (rows > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "B*H*Nq too large");
     dim3 grid((unsigned)((rows + kThreads / 32 - 1) / (kThreads / 32)));
-    if (o_dtype == ATTN_DTYPE_BF16)
-        merge_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, rs, ss,
-                                                               (int)dv, static_cast<__nv_bfloat16 *>(o),
-                                                               o_stride[0], o_stride[1], o_stride[2], lse);
-    else
-        merge_kernel<float><<<grid, kThreads, 0, st>>>(partials, rows, (int)H, (int)Nq, num_splits, rs, ss,
-                                                       (int)dv, static_cast<float *>(o), o_stride[0],
-                                                       o_stride[1], o_stride[2], lse);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e =
+        o_dtype == ATTN_DTYPE_BF16
+            ? launch_pdl(merge_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, st, partials, rows, (int)H, (int)Nq,
+                         num_splits, rs, ss, (int)dv, static_cast<__nv_bfloat16 *>(o), o_stride[0], o_stride[1],
+                         o_stride[2], lse)
+            : launch_pdl(merge_kernel<float>, grid, dim3(kThreads), 0, st, partials, rows, (int)H, (int)Nq,
+                         num_splits, rs, ss, (int)dv, static_cast<float *>(o), o_stride[0], o_stride[1],
+                         o_stride[2], lse);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }

@@ -183,6 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
         ptx::prefetch_tmap(&tm_o);
+        // launched as a programmatic dependent of the previous kernel in the stream: nothing
+        // in global memory is read before that kernel has completed
+        ptx::grid_dep_wait();
         // this thread is the producer: the first item's Q_A and K_0 start loading before the
         // tensor-memory allocation and the block barrier
         const Item it = next_item<kPartial>(a, dr, -1, cta, G, total);
@@ -207,10 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(&ctrl->tmem_base, kTmemCols);
         ptx::tmem_relinquish();
     }
+    ptx::grid_dep_wait();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
+    // the next kernel in the stream may be scheduled onto SMs as this grid's CTAs finish: its
+    // set-up then overlaps this grid's tail (it reads global memory only after this grid
+    // has completed)
+    ptx::launch_dependents();
 
     // Barrier phases run on from one item to the next: g counts key tiles (K/V ring slots),
     // and per query tile, Q loads, S/P hand-offs and finished items are counted likewise.
@@ -550,8 +558,7 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     const int sms = sm_count();
     if (sms <= 0) return fail(ATTN_ERR_CUDA, "could not read the SM count");
     const unsigned grid = (unsigned)(total < sms ? total : sms);
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, a, dr);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, mq, mk, mv, mo, a, dr);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16_pair launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }

@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort = &ctrl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // launched as a programmatic dependent of the previous kernel in the stream: nothing in
+    // global memory is read before that kernel has completed
+    ptx::grid_dep_wait();
     // work items longest first: later query tiles (causal ones see more keys) first, or, with
     // per-sequence key lengths, longer sequences first
     int qt, b, h;
@@ -212,6 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
+    // the next kernel in the stream may be scheduled once every CTA of this grid has started
+    ptx::launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: Q, K
@@ -515,8 +520,7 @@ attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     auto kern = fwd_bf16_kernel<DK, DV, kBias, kTmaBias>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mb, mo, a);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, mq, mk, mv, mb, mo, a);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "fwd_bf16 launch: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }
