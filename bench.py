@@ -456,7 +456,8 @@ def run_ours(args):
     # ---------------------------------------------------------------- the headline: 2k causal
     a = wl.causal_2k(dev)
     flops = a.flops()
-    head_src = ("fwd_bf16_pair_sm103.cu", "fwd_bf16_common.cuh", "sm100_ptx.cuh")
+    head_src = ("fwd_bf16_pair_sm103.cu", "fwd_bf16_common.cuh", "sm100_ptx.cuh", "dropout_rng.cuh",
+                "attn_internal.h")
     head = prefill_object(ofa, a, args, stream, pk, pk_kind, windows, barrier, world, dev, 4, "tensor",
                           profiled_traffic("fwd_bf16_pair_kernel.causal_b4_h16_n2048_d128.md", head_src))
     ms = head["ms_per_step"]
@@ -547,7 +548,8 @@ def run_ours(args):
         extra["padbias"] = prefill_object(
             ofa, pb, args, stream, pk, pk_kind, other_windows, barrier, world, dev, 3, "combined",
             profiled_traffic("fwd_bf16_kernel.padbias_b8_h8_n1024_dk192_dv128.md",
-                             ("fwd_bf16_sm103.cu", "fwd_bf16_common.cuh", "sm100_ptx.cuh")))
+                             ("fwd_bf16_sm103.cu", "fwd_bf16_common.cuh", "sm100_ptx.cuh",
+                              "dropout_rng.cuh", "attn_internal.h")))
         if rank == 0 and not args.no_cpu:
             val, secs, desc, threads, _ = cpu_oracle_sample(pb, args.cpu_seconds / 2, seed=1)
             extra["padbias"]["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
@@ -606,7 +608,8 @@ def run_ours(args):
                             "read_peak_kind": "torch sum over 4 GiB, this run (read only)",
                             "frac_nominal": gbs / NOMINAL["hbm_gbs"],
                             "traffic": profiled_traffic("decode_split_kernel.decode_b64_h32_l8192_d128.md",
-                                                        ("decode.cu",))}}
+                                                        ("decode.cu", "sm100_ptx.cuh", "warp_mma.cuh",
+                                                         "attn_internal.h"))}}
         del d, ws, wsf
 
     # backward of the same workload (dQ, dK, dV from o, lse and a seeded random dO): reported
@@ -614,47 +617,47 @@ def run_ours(args):
     # step (row terms, products, dQ conversion: three launches)
     bwd = None
     if not args.no_backward:
+        # three copies of the step's inputs (q, k, v, o, lse, dO) with gradients of their own
+        # (about 400 MB, over three times L2), stepped back to back like the forward
         o_b, l_b = ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale)
         gen = torch.Generator(device=dev)
         gen.manual_seed(7)
         dout_b = torch.randn(o_b.shape, generator=gen, device=dev).to(o_b.dtype)
         ws_b = torch.empty(ofa.bwd_workspace_bytes(a.B, a.H, a.Nq, a.dk) // 4 + 4, dtype=torch.float32,
                            device=dev)
-        gq, gk, gv = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
-        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        n_bsets = 3
+        bsets = []
+        for t in range(n_bsets):
+            cp = (lambda x: x if t == 0 else x.clone())
+            bsets.append((cp(a.q), cp(a.k), cp(a.v), cp(o_b), cp(l_b), cp(dout_b),
+                          torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)))
 
-        def bstep():
-            ofa.attn_bwd(a.q, a.k, a.v, o_b, l_b, dout_b, causal=True, scale=a.scale, dq=gq, dk=gk, dv=gv,
+        def bstep(n):
+            q_, k_, v_, o_, l_, g_, dq_, dk_, dv_ = bsets[n % n_bsets]
+            ofa.attn_bwd(q_, k_, v_, o_, l_, g_, causal=True, scale=a.scale, dq=dq_, dk=dk_, dv=dv_,
                          workspace=ws_b)
 
-        for _ in range(max(3, min(args.warmup, 10))):
-            flush.zero_()
-            bstep()
-        nb = max(5, min(args.steps, 50))
-        evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
-        barrier()
-        t0 = time.time()
-        for s_, e_ in evb:
-            flush.zero_()            # L2 flush, outside the timed interval
-            s_.record(stream)
-            bstep()
-            e_.record(stream)
-        barrier()
-        other_windows.append((t0, time.time()))
+        est_b = warm(bstep, max(3, args.warmup), stream)
+        ofa.device_error_flags()
+        ms_b, reps_b = time_steps(bstep, args.steps, stream, args.min_seconds, est_b, barrier, other_windows)
         if ofa.device_error_flags() & 1:
             raise RuntimeError("a backward kernel gave up a bounded wait during the timed region")
-        ms_b = max_over_ranks(sum(s_.elapsed_time(e_) for s_, e_ in evb) / nb, world, dev)
+        ms_b = max_over_ranks(ms_b, world, dev)
         bflops = a.visible_pairs() * (6 * a.dk + 4 * a.dv)   # five products per visible pair
         tb = job_rate(1, bflops, ms_b)
         bwd = {"workload": "bf16_causal_b4_h16_n2048_d128_backward", "value": job_rate(world, bflops, ms_b),
-               "unit": "TFLOP/s", "ms_per_step": ms_b, "steps": nb, "flops_per_step": bflops,
-               "gpu_launches_per_step": 3, "l2": "flushed before every step",
+               "unit": "TFLOP/s", "ms_per_step": ms_b, "steps": args.steps, "repeats": reps_b,
+               "flops_per_step": bflops, "gpu_launches_per_step": 3,
+               "l2": f"inputs rotated over {n_bsets} copies (about 400 MB > 129 MB L2), no flush",
                "roofline": {"bound": "tensor", "achieved": tb, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": tb / pk["bf16_tflops"], "peak_kind": f"{pk_kind} dense bf16 (burst)",
                             "frac_nominal": tb / NOMINAL["bf16_tflops"],
                             "over": "the whole backward step (bwd_prep_kernel, bwd_tc_kernel, bwd_dq_kernel)",
-                            "traffic": None}}
-        del o_b, l_b, dout_b, ws_b, gq, gk, gv, flush
+                            "traffic": profiled_traffic("bwd_tc_kernel.causal_b4_h16_n2048_d128.md",
+                                                        ("bwd_tc_sm103.cu", "sm100_ptx.cuh", "fwd_bf16_common.cuh",
+                                                         "dropout_rng.cuh", "attn_internal.h")),
+                            "traffic_kernel": "bwd_tc_kernel (its DRAM bytes per launch)"}}
+        del o_b, l_b, dout_b, ws_b, bsets
 
     clocks = clk.stop(windows)
     clk_all = None
