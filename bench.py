@@ -413,6 +413,7 @@ def prefill_object(ofa, a, args, stream, pk, pk_kind, clk_windows, barrier, worl
     if roof_kind == "tensor":
         obj["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                            "frac": tflops / pk["bf16_tflops"], "peak_kind": f"{pk_kind} dense bf16 (burst)",
+                           "frac_sustained": tflops / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
                            "frac_nominal": tflops / NOMINAL["bf16_tflops"], "traffic": traffic}
     else:
         # bytes-bound: the roofline time is max(FLOPs / tensor peak, bytes / HBM peak)
