@@ -728,6 +728,8 @@ CASES = {
     "bwd_dropout": ("causal_2k", {}, "bwd_dropout"),
     "bwd_dropout_rng": ("causal_2k", {}, "bwd_dropout_rng"),
     "bwd_long": ("long_causal", {"H": 8}, "bwd"),
+    "bwd_d64": ("causal_2k", {"d": 64}, "bwd"),
+    "bwd_bias": ("causal_2k", {"bias": True, "B": 2, "H": 8}, "bwd"),
 }
 
 

@@ -341,9 +341,9 @@ extern "C" attn_status_t attn_bwd(const attn_bwd_params_t *p, void *workspace, s
     attn_status_t st = check_common(f);
     if (st) return st;
     if (f->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward supports bfloat16 only");
-    if (has_dropout(f)) {  // the backward of a dropout forward runs on the d = 128 tcgen05 kernel
-        if (f->dk != 128 || f->dv != 128 || f->bias)
-            return fail(ATTN_ERR_UNSUPPORTED, "the backward of a dropout forward supports dk = dv = 128 without a bias");
+    if (has_dropout(f)) {  // the backward of a dropout forward runs on the tcgen05 kernel
+        if (f->bias)
+            return fail(ATTN_ERR_UNSUPPORTED, "the backward of a dropout forward takes no bias");
         if (f->dropout_mask && (!aligned16(f->dropout_mask) || !stride_mult(f->dropout_mask_stride, 16)))
             return fail(ATTN_ERR_MISALIGNED, "dropout_mask must be 16-byte aligned with strides that are multiples of 16 bytes");
     }

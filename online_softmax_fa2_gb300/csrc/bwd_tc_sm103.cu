@@ -1,5 +1,5 @@
-// bwd_tc_sm103.cu -- attention backward for dk == dv == 128 (no bias) on the 5th-generation
-// tensor cores.
+// bwd_tc_sm103.cu -- attention backward for dk == dv in {64, 128} on the 5th-generation tensor
+// cores.
 //
 // The same gradients as bwd.cu ("How Does FlashAttention Preserve Global Softmax Across
 // Tiles?", section 7: rebuild p_ij = exp(x_ij - L_i), c_i = g_i . o_i, dS_ij = p_ij (g_i . v_j -
@@ -57,7 +57,10 @@ struct TcArgs {
     const float *lrow;  // [B, H, nq_pad]: lse * log2 e, rows padded to a multiple of 128
     int nq_pad;
     const int *kv_lens;
-    float *dq_acc;  // [B, Nq, H, 128]
+    const float *bias;  // [B, H, Nq, Nk] with element strides bs0, bs1, bs2 (key stride 1), or null
+    long long bs0, bs1, bs2;
+    int bias_pf;        // bias rows 16-byte aligned: the producer prefetches them into L2
+    float *dq_acc;  // [B, Nq, H, D]
     __nv_bfloat16 *dk, *dv;
     long long dks0, dks1, dks2, dvs0, dvs1, dvs2;
     uint32_t *flags;
@@ -111,6 +114,19 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, f
 }  // namespace ptx
 namespace {
 
+// A read-only load that the compiler keeps where it is written (so that a batch of them is in
+// flight before the values are used)
+__device__ __forceinline__ float ld_nc_f32(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -138,7 +154,16 @@ __device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
 // kDrop: the forward ran with dropout; `dr` holds its keep bits (bit j % 8 of byte j / 8 of a
 // row) and 1 / (1 - p).  The gradient reaching P then carries the mask and its scale: the
 // stored P^T (for dV) is z p / (1 - p), and dS = p (z dP / (1 - p) - c).
-template <bool kDrop>
+//
+// D is the head dimension (dk = dv = D, 64 or 128).  With D = 64 only the first 64-column
+// panel of Q, V and G is loaded and the products over the head dimension take half the
+// steps; K's second panel is filled with zeros by the copy (its columns lie past the tensor),
+// so that dQ^T = K^T dS^T keeps M = 128 and its rows 64 .. 127 come out zero.
+//
+// kBias: the forward's bias is added to the logits before the exponential.  The transform
+// thread of key j reads b_ij of the 32 rows of a chunk before it waits for the chunk's S^T
+// (for each row the warp's 32 keys are one 128-byte line).
+template <bool kDrop, int D, bool kBias>
 __global__ void __launch_bounds__(kTcThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -174,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (j < a.Nk) {
                 uint4 *dkr = reinterpret_cast<uint4 *>(a.dk + b * a.dks0 + (long long)j * a.dks1 + h * a.dks2);
                 uint4 *dvr = reinterpret_cast<uint4 *>(a.dv + b * a.dvs0 + (long long)j * a.dvs1 + h * a.dvs2);
-                for (int c = 0; c < 16; ++c) dkr[c] = dvr[c] = make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < D / 8; ++c) dkr[c] = dvr[c] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         return;
@@ -200,13 +225,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
         ptx::prefetch_tmap(&tm_g);
-        ptx::mbar_arrive_expect_tx(&ctrl->kv_full, 2 * kTile);
-        for (int p = 0; p < 2; ++p) {
+        // K in two panels always (with D = 64 the second is zero-filled), V, Q and G in D / 64
+        ptx::mbar_arrive_expect_tx(&ctrl->kv_full, (2 + D / 64) * kPanelBytes);
+        for (int p = 0; p < 2; ++p)
             ptx::tma_load_4d(smem + kOffK + p * kPanelBytes, &tm_k, &ctrl->kv_full, p * 64, j0, h, b);
+        for (int p = 0; p < D / 64; ++p)
             ptx::tma_load_4d(smem + kOffV + p * kPanelBytes, &tm_v, &ctrl->kv_full, p * 64, j0, h, b);
-        }
-        ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], 2 * kTile + 512);
-        for (int p = 0; p < 2; ++p) {
+        ptx::mbar_arrive_expect_tx(&ctrl->q_full[0], 2 * (D / 64) * kPanelBytes + 512);
+        for (int p = 0; p < D / 64; ++p) {
             ptx::tma_load_4d(smem + kOffQ + p * kPanelBytes, &tm_q, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
             ptx::tma_load_4d(smem + kOffG + p * kPanelBytes, &tm_g, &ctrl->q_full[0], p * 64, t_first * BQ, h, b);
         }
@@ -227,20 +253,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return ptx::mbar_wait(bar, parity, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
     };
     const int ntiles = t_end - t_first;
+    // the bias rows of query tile t over this block's keys into L2 (ahead of the transform's loads)
+    auto prefetch_bias = [&](int t) {
+        if constexpr (kBias) {
+            if (!a.bias_pf) return;
+            const uint32_t bytes = (uint32_t)((min(a.Nk, j0 + BK) - j0) * 4) & ~15u;
+            if (bytes == 0) return;
+            const float *base = a.bias + b * a.bs0 + h * a.bs1 + j0;
+            for (int i = t * BQ; i < min(a.Nq, t * BQ + BQ); ++i) prefetch_l2(base + (long long)i * a.bs2, bytes);
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int loaded = 1;
+            prefetch_bias(t_first);
             // tile k into stage k & 1, once the products of tile k - 2 have read that stage
             for (int k = 1; k < ntiles; ++k) {
                 const int st = k & 1;
                 if (k >= 2 && !wait(&ctrl->q_empty[st], ((k >> 1) - 1) & 1)) break;
                 const int i0 = (t_first + k) * BQ;
-                ptx::mbar_arrive_expect_tx(&ctrl->q_full[st], 2 * kTile + 512);
+                prefetch_bias(t_first + k);
+                ptx::mbar_arrive_expect_tx(&ctrl->q_full[st], 2 * (D / 64) * kPanelBytes + 512);
                 bulk_load(smem + kOffL + st * 512, a.lrow + ((long long)b * a.H + h) * a.nq_pad + i0, 512,
                           &ctrl->q_full[st]);
-                for (int p = 0; p < 2; ++p) {
+                for (int p = 0; p < D / 64; ++p) {
                     ptx::tma_load_4d(smem + kOffQ + st * kTile + p * kPanelBytes, &tm_q, &ctrl->q_full[st], p * 64, i0,
                                      h, b);
                     ptx::tma_load_4d(smem + kOffG + st * kTile + p * kPanelBytes, &tm_g, &ctrl->q_full[st], p * 64, i0,
@@ -258,7 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ tensor-core issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_ab(BK, kHalf, false, false);  // S^T, dP^T of a half
-            constexpr uint32_t kIdKV = idesc_ab(BK, 128, false, true);    // dV, dK: A from TMEM, B MN-major
+            constexpr uint32_t kIdKV = idesc_ab(BK, D, false, true);      // dV, dK: A from TMEM, B MN-major
             constexpr uint32_t kIdQ = idesc_ab(128, kHalf, true, true);   // dQ^T: A and B MN-major
             const uint32_t sK = ptx::smem_u32(smem + kOffK), sV = ptx::smem_u32(smem + kOffV);
             const uint32_t sS = ptx::smem_u32(smem + kOffS);
@@ -275,14 +313,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint64_t qd = ptx::sdesc_sw128(ptx::smem_u32(smem + off_q), 16, 1024);
                 const uint64_t gd = ptx::sdesc_sw128(ptx::smem_u32(smem + off_g), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
                     ptx::mma_ss(tmem + hh * kHalf, kd + off, qd + off, kIdS, kk > 0 ? 1u : 0u);
                 }
                 if (k > 0 && !wait(&ctrl->dq_free[hh], (k - 1) & 1)) return false;
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
                     ptx::mma_ss(tmem + 128 + hh * kHalf, vd + off, gd + off, kIdS, kk > 0 ? 1u : 0u);
                 }
@@ -401,7 +439,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
+            // bias: the 32 rows of chunk c at this thread's key, issued one chunk ahead of use
+            // (rows and keys past the ends read row Nq - 1 / key Nk - 1; those weights are
+            // selected away)
+            float bv[kBias ? 32 : 1];
+            auto load_bias = [&](int c) {
+                if constexpr (kBias) {
+                    const float *bcol = a.bias + b * a.bs0 + h * a.bs1 + min(j, a.Nk - 1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        bv[e] = ld_nc_f32(bcol + (long long)min(i0 + 32 * c + e, a.Nq - 1) * a.bs2);
+                }
+            };
             for (int hh = 0; ok && hh < 2; ++hh) {
+            load_bias(2 * hh);  // in flight during the wait for S^T
             // s_full implies the tile's copies are done; waiting on their barrier as well makes
             // the copied L visible to these threads
             if (!wait_warp(&ctrl->s_full[hh], k & 1) || !wait_warp(&ctrl->q_full[k & 1], (k >> 1) & 1) ||
@@ -432,6 +483,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float x0, x1, g0, g1;
                     ptx::fma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), a.scale_log2, a.scale_log2,
                               -L2.x, -L2.y);
+                    if constexpr (kBias) ptx::fma2(x0, x1, bv[e], bv[e + 1], kLog2e, kLog2e, x0, x1);
                     float zs0 = 1.f, zs1 = 1.f;  // z / (1 - p) of rows e, e + 1 for this key
                     if constexpr (kDrop) {
                         const uint32_t w0 = __shfl_sync(0xffffffffu, Zt, e), w1 = __shfl_sync(0xffffffffu, Zt, e + 1);
@@ -444,8 +496,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int i = i0 + 32 * c + e;
                     // visibility of rows i and i + 1 (selects, not products: anything stored past
                     // the sequence, NaN included, is dropped)
-                    const bool v0 = j < n && i < a.Nq && (!a.causal || j <= i + shift);
-                    const bool v1 = j < n && i + 1 < a.Nq && (!a.causal || j <= i + 1 + shift);
+                    bool v0 = j < n && i < a.Nq && (!a.causal || j <= i + shift);
+                    bool v1 = j < n && i + 1 < a.Nq && (!a.causal || j <= i + 1 + shift);
+                    if constexpr (kBias) {  // a -inf bias masks the key (a row it empties has L = -inf)
+                        v0 = v0 && bv[e] != -INFINITY;
+                        v1 = v1 && bv[e + 1] != -INFINITY;
+                    }
                     const float p0 = v0 ? ptx::ex2(x0) : 0.f, p1 = v1 ? ptx::ex2(x1) : 0.f;
                     float d0, d1;
                     ptx::mul2(d0, d1, p0, p1, g0, g1);
@@ -458,6 +514,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     dp[e / 2] = ptx::pack_bf16x2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
                 }
+                if (c == 2 * hh) load_bias(c + 1);  // the next chunk's, while this one is stored
                 // P^T and dS^T of the half packed into the first 32 of its S^T and dP^T columns
                 // (all read by now: chunk 2hh + 1 packs over chunk 2hh)
                 tmem_st16(lane_addr + 32 * hh + 16 * c, pp);
@@ -484,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __nv_bfloat16 *dkr = a.dk + b * a.dks0 + (long long)j * a.dks1 + h * a.dks2;
             __nv_bfloat16 *dvr = a.dv + b * a.dvs0 + (long long)j * a.dvs1 + h * a.dvs2;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t kv[32], vv[32];
                 ptx::tmem_ld32(lane_addr + 384 + 32 * c, kv);
                 ptx::tmem_ld32(lane_addr + 256 + 32 * c, vv);
@@ -514,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ dQ^T (one head dimension each)
         const int d = (int)threadIdx.x - 256;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const long long row_stride = (long long)a.H * 128;
+        const long long row_stride = (long long)a.H * D;
         ptx::grid_dep_wait();
         bool ok = true;
         for (int k = 0; ok && k < ntiles; ++k) {
@@ -526,7 +583,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const int i0 = (t_first + k) * BQ + hh * kHalf, rows = min(kHalf, a.Nq - i0);
-                float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * 128 + (d & ~3);
+                float *dst = a.dq_acc + (((long long)b * a.Nq + i0) * a.H + h) * D + (d & ~3);
                 // the half's 64 rows of this dimension into registers first, so the columns are
                 // free for the next tile's dP^T before the reductions are issued
                 uint32_t qv[2][32];
@@ -546,7 +603,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int t = 0; t < 4; ++t) x[t] = a.scale * __uint_as_float(qv[m / 8][4 * (m % 8) + t]);
                     transpose4(x, lane);
                     const int row = 4 * m + (lane & 3);
-                    if (row < rows) red_add_v4(dst + row * row_stride, x[0], x[1], x[2], x[3]);
+                    if (d < D && row < rows) red_add_v4(dst + row * row_stride, x[0], x[1], x[2], x[3]);
                 }
             }
         }
@@ -568,16 +625,26 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     const attn_fwd_params_t &f = p.fwd;
     CUtensorMap mq, mk, mv, mg;
     attn_status_t st;
-    if ((st = encode(&mq, f.q, f.B, f.Nq, f.H, 128, f.q_stride, "q")) ||
-        (st = encode(&mk, f.k, f.B, f.Nk, f.H, 128, f.k_stride, "k")) ||
-        (st = encode(&mv, f.v, f.B, f.Nk, f.H, 128, f.v_stride, "v")) ||
-        (st = encode(&mg, p.dout, f.B, f.Nq, f.H, 128, p.dout_stride, "dout")))
+    if (f.dk != f.dv || (f.dk != 64 && f.dk != 128))
+        return fail(ATTN_ERR_UNSUPPORTED, "the tcgen05 backward supports dk == dv in {64, 128}");
+    if ((st = encode(&mq, f.q, f.B, f.Nq, f.H, f.dk, f.q_stride, "q")) ||
+        (st = encode(&mk, f.k, f.B, f.Nk, f.H, f.dk, f.k_stride, "k")) ||
+        (st = encode(&mv, f.v, f.B, f.Nk, f.H, f.dv, f.v_stride, "v")) ||
+        (st = encode(&mg, p.dout, f.B, f.Nq, f.H, f.dv, p.dout_stride, "dout")))
         return st;
     TcArgs a;
     a.B = (int)f.B; a.H = (int)f.H; a.Nq = (int)f.Nq; a.Nk = (int)f.Nk; a.causal = f.causal;
     a.scale = f.scale; a.scale_log2 = f.scale * kLog2e;
     a.crow = crow; a.lrow = lrow; a.nq_pad = (int)((f.Nq + 127) / 128 * 128);
     a.kv_lens = f.kv_lens; a.dq_acc = dq_acc;
+    a.bias = f.bias;
+    a.bs0 = f.bias_stride[0]; a.bs1 = f.bias_stride[1]; a.bs2 = f.bias_stride[2];
+    {
+        const int64_t sizes[3] = {f.B, f.H, f.Nq};
+        bool pf = f.bias && (reinterpret_cast<uintptr_t>(f.bias) & 15u) == 0;
+        for (int t = 0; t < 3; ++t) pf = pf && (sizes[t] <= 1 || f.bias_stride[t] % 4 == 0);
+        a.bias_pf = pf ? 1 : 0;
+    }
     a.dk = static_cast<__nv_bfloat16 *>(p.dk);
     a.dv = static_cast<__nv_bfloat16 *>(p.dv);
     a.dks0 = p.dk_stride[0]; a.dks1 = p.dk_stride[1]; a.dks2 = p.dk_stride[2];
@@ -586,7 +653,14 @@ attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const flo
     if (!a.flags) return fail(ATTN_ERR_CUDA, "could not resolve the device error word");
     bf16fwd::DropArgs dr{};
     fill_dropout(dr, f);
-    auto kernel = (dr.dmask || dr.rng) ? bwd_tc_kernel<true> : bwd_tc_kernel<false>;
+    const bool drop = dr.dmask || dr.rng;
+    if (drop && f.bias) return fail(ATTN_ERR_UNSUPPORTED, "the backward of a dropout forward takes no bias");
+    auto kernel = f.dk == 64 ? (drop     ? bwd_tc_kernel<true, 64, false>
+                                : f.bias ? bwd_tc_kernel<false, 64, true>
+                                         : bwd_tc_kernel<false, 64, false>)
+                             : (drop     ? bwd_tc_kernel<true, 128, false>
+                                : f.bias ? bwd_tc_kernel<false, 128, true>
+                                         : bwd_tc_kernel<false, 128, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     if ((f.Nk + BK - 1) / BK > 65535 || f.B > 65535)

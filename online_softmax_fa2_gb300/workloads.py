@@ -152,9 +152,11 @@ def fp32_small(device="cpu", seed=0):
                         name="fp32_b1_h1_n128_d64")
 
 
-def causal_2k(device="cpu", seed=1):
-    return make_prefill(4, 16, 2048, 2048, 128, 128, torch.bfloat16, causal=True, seed=seed,
-                        device=device, name="bf16_causal_b4_h16_n2048_d128")
+def causal_2k(device="cpu", seed=1, d=128, bias=False, B=4, H=16):
+    """The 2k causal workload (B4 H16 d128); d, bias, B and H give its variants."""
+    name = f"bf16_causal_b{B}_h{H}_n2048_d{d}" + ("_bias" if bias else "")
+    return make_prefill(B, H, 2048, 2048, d, d, torch.bfloat16, causal=True, bias=bias, seed=seed,
+                        device=device, name=name)
 
 
 def padded_bias(device="cpu", seed=2, poison=True):

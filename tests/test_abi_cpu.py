@@ -206,8 +206,7 @@ def test_decode_refuses_and_bwd_restricts_a_dropout_mask(lib):
         return b
     wsb = ctypes.c_void_p(0xB0000)
     need = lib.attn_bwd_workspace_bytes(1, 1, 64, 64)
-    # the backward of a dropout forward runs on the d = 128 kernel without a bias only
-    assert lib.attn_bwd(ctypes.byref(bp(dk=64, dv=64)), wsb, need, None) == ofa.Status.UNSUPPORTED
+    # the backward of a dropout forward takes no bias
     b = bp()
     b.fwd.bias = 0xC0000
     assert lib.attn_bwd(ctypes.byref(b), wsb, 1 << 20, None) == ofa.Status.UNSUPPORTED

@@ -77,9 +77,10 @@ def test_bwd_matches_oracle(d, causal, Nq, Nk):
     check_all(a, dq, dk, dv, rq, rk, rv, f"d={d} causal={causal} {Nq}x{Nk}", dout)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_padding_bias_and_masks(causal):
-    a = wl.make_prefill(4, 2, 130, 200, 128, 128, torch.bfloat16, causal=causal, bias=True,
+def test_bwd_padding_bias_and_masks(causal, d):
+    a = wl.make_prefill(4, 2, 130, 200, d, d, torch.bfloat16, causal=causal, bias=True,
                         kv_lens=[200, 0, 65, 1], seed=61, device=DEV, bias_mask_p=0.05)
     dout, dq, dk, dv = run_bwd(a, 1)
     rq, rk, rv = oracle_bwd(a, dout)
@@ -96,6 +97,24 @@ def test_bwd_dk_dv_deterministic_and_poison_free():
     assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2
     # keys past kv_len hold NaN (the workload's poison): no gradient reads them
     assert torch.isfinite(dq1.float()).all() and torch.isfinite(dk1.float()).all()
+
+
+@pytest.mark.parametrize("d,bias", [(64, False), (128, True)])
+def test_bwd_full_size_shapes_sampled_heads(d, bias):
+    # the 2k causal shape at d = 64, and at d = 128 with a broadcast-free fp32 bias (two heads
+    # against the oracle each)
+    a = wl.make_prefill(2, 8, 2048, 2048, d, d, torch.bfloat16, causal=True, bias=bias, seed=63, device=DEV)
+    dout, dq, dk, dv = run_bwd(a, 4)
+    o = run_bwd.last_o
+    for b, h in ((0, 0), (1, 7)):
+        sub = lambda t: cpu32(t[b:b + 1, :, h:h + 1])
+        bsub = cpu32(a.bias[b:b + 1, h:h + 1]) if bias else None
+        rq, rk, rv, _ = oracle.attn_bwd(sub(a.q), sub(a.k), sub(a.v), sub(dout), bias=bsub, causal=True,
+                                        scale=a.scale)
+        ct = dq_c_term(sub(dout), sub(o), sub(a.k), a.scale)
+        check_grad(dq[b:b + 1, :, h:h + 1], rq, f"dq d={d} bias={bias} head {b},{h}", extra=ct)
+        check_grad(dk[b:b + 1, :, h:h + 1], rk, f"dk d={d} bias={bias} head {b},{h}")
+        check_grad(dv[b:b + 1, :, h:h + 1], rv, f"dv d={d} bias={bias} head {b},{h}")
 
 
 def test_bwd_causal_b4_h16_n2048_d128_sampled_heads():

@@ -108,9 +108,10 @@ def run_bwd_drop(a, keep, p, seed=0):
     return dout, grads
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal,p,lens", [(True, 0.2, [333, 170]), (False, 0.5, [301, 333])])
-def test_bwd_dropout_matches_oracle(causal, p, lens):
-    a = wl.make_prefill(2, 2, 300, 333, 128, 128, torch.bfloat16, causal=causal, kv_lens=lens, seed=45,
+def test_bwd_dropout_matches_oracle(causal, p, lens, d):
+    a = wl.make_prefill(2, 2, 300, 333, d, d, torch.bfloat16, causal=causal, kv_lens=lens, seed=45,
                         device=DEV)
     keep = wl.dropout_keep(a.B, a.H, a.Nq, a.Nk, p, seed=11, device=DEV)
     dout, grads = run_bwd_drop(a, keep, p)
@@ -200,9 +201,10 @@ def test_fp32_in_kernel_draws_equal_the_oracles_generator():
     assert np.max(np.abs(o1.cpu().numpy() - o_ref)) <= 1e-5 / (1.0 - p_real)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal,p,lens", [(True, 0.2, [333, 170]), (False, 0.5, [301, 333])])
-def test_bwd_in_kernel_draws_match_oracle(causal, p, lens):
-    a = wl.make_prefill(2, 2, 300, 333, 128, 128, torch.bfloat16, causal=causal, kv_lens=lens, seed=49,
+def test_bwd_in_kernel_draws_match_oracle(causal, p, lens, d):
+    a = wl.make_prefill(2, 2, 300, 333, d, d, torch.bfloat16, causal=causal, kv_lens=lens, seed=49,
                         device=DEV)
     seed, offset = 1234567, 5
     o, lse = ofa.attn_fwd(a.q, a.k, a.v, kv_lens=a.kv_lens, causal=causal, scale=a.scale, dropout_p=p,
