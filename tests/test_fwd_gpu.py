@@ -91,7 +91,7 @@ def test_fp32_head_dims_256():
 
 # ------------------------------------------------------------------------ bfloat16 path
 
-DIMS = [(64, 64), (128, 128), (192, 128), (128, 64), (64, 128)]
+DIMS = [(64, 64), (128, 128), (192, 128), (192, 64), (128, 64), (64, 128)]
 
 
 @pytest.mark.parametrize("dk,dv", DIMS)
@@ -103,6 +103,22 @@ def test_bf16_multi_tile_ragged(dk, dv, causal):
     o, lse = run(a)
     o_ref, l_ref, _ = oracle_full(a)
     compare(o, lse, o_ref, l_ref, torch.bfloat16, empty=empty_rows(a), what=f"bf16 {dk}/{dv}")
+
+
+@pytest.mark.parametrize("B,causal,bias", [(40, True, False), (12, False, True)])
+def test_bf16_dk192_many_items_per_cta(B, causal, bias):
+    # the persistent dk = 192 kernel walks several items per CTA: per-sequence lengths with
+    # empty and one-key sequences, more than 32 sequences (no length ranking) or fewer, and
+    # every ring running on across items; rows spread over all sequences are checked
+    lens = [(37 * b) % 400 for b in range(B)]
+    lens[1], lens[2] = 0, 1
+    a = wl.make_prefill(B, 3, 390, 400, 192, 128, torch.bfloat16, causal=causal, bias=bias, kv_lens=lens,
+                        seed=25, device=DEV)
+    o, lse = run(a)
+    rows = sample_rows(a, n_per_head=24, heads=[(b, h) for b in range(B) for h in range(3)])
+    o_ref, l_ref, _ = oracle_full(a, rows=rows)
+    o_s, l_s = gather_rows(o, lse, rows, a.H, a.Nq)
+    compare_rows(o_s, l_s, o_ref, l_ref, torch.bfloat16, what=f"dk192 B={B} causal={causal} bias={bias}")
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (192, 128)])
