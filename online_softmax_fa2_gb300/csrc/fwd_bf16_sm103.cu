@@ -531,6 +531,11 @@ attn_status_t dispatch(int dk, int dv, const CUtensorMap &mq, const CUtensorMap 
                        cudaStream_t s) {
     if (dk == 192 && dv == 128) return launch_t<192, 128, kBias, kTmaBias>(mq, mk, mv, mb, mo, a, grid, s);
     if (dk == 192 && dv == 64) return launch_t<192, 64, kBias, kTmaBias>(mq, mk, mv, mb, mo, a, grid, s);
+    if constexpr (kTmaBias) {  // dk <= 128 with a staged bias (the output tile fits in Q's buffer)
+        if (dk == 128 && dv == 128) return launch_t<128, 128, true, true>(mq, mk, mv, mb, mo, a, grid, s);
+        if (dk == 128 && dv == 64) return launch_t<128, 64, true, true>(mq, mk, mv, mb, mo, a, grid, s);
+        if (dk == 64 && dv == 64) return launch_t<64, 64, true, true>(mq, mk, mv, mb, mo, a, grid, s);
+    }
     return fail(ATTN_ERR_UNSUPPORTED, "no one-tile bf16 kernel for dk=%d dv=%d", dk, dv);
 }
 
@@ -552,8 +557,14 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
         mk = mq;  // never read: with no keys every tile is empty
         mv = mq;
     }
-    // dk <= 128: two query tiles per CTA; dk = 192: one (two would not fit in shared memory)
-    const bool pair = p.dk <= 128;
+    // dk <= 128: two query tiles per CTA; dk = 192: one (two would not fit in shared memory).
+    // With a bias that TMA can stage (and no dropout), dk >= dv <= 128 also takes the one-tile
+    // kernel: its bias streams through shared memory in panels, which the two-tile kernel has
+    // no room for (it reads each row's bias into registers)
+    CUtensorMap mb = mq;  // read only by kernels that stage the bias
+    const bool staged_bias = p.bias && p.Nk > 0 && encode_bias(&mb, p);
+    const bool drop = p.dropout_mask || p.dropout_rng == 1;
+    const bool pair = p.dk <= 128 && !(staged_bias && !drop && p.dk >= p.dv);
     Args a;
     a.B = (int)p.B; a.H = (int)p.H; a.Nq = (int)p.Nq; a.Nk = (int)p.Nk; a.causal = p.causal;
     a.n_items = (int)((p.Nq + (pair ? 2 * BQ : BQ) - 1) / (pair ? 2 * BQ : BQ));
@@ -576,9 +587,7 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     if (dr.dmask || dr.rng) return fail(ATTN_ERR_UNSUPPORTED, "dropout with dk = %lld is not built", (long long)p.dk);
     const long long grid = (long long)a.n_items * p.B * p.H;
     if (grid > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many query tiles");
-    CUtensorMap mb = mq;  // read only by kernels that stage the bias
-    if (p.bias && p.Nk > 0 && encode_bias(&mb, p))
-        return dispatch<true, true>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
+    if (staged_bias) return dispatch<true, true>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
     if (p.bias) return dispatch<true, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
     return dispatch<false, false>((int)p.dk, (int)p.dv, mq, mk, mv, mb, mo, a, (unsigned)grid, s);
 }
