@@ -261,13 +261,14 @@ __device__ __forceinline__ void scale_o(uint32_t taddr, float alpha) {
     ptx::tmem_st_wait();
 }
 
-// Divide once: o = u / l rounded to bf16 into orow (skipped when orow is null: a row past Nq),
-// lse = (m + log2 l) * ln 2.  An empty row (l == 0) gives +0.0 and -inf.  Warp-collective.
+// Divide once: o = g u / l rounded to bf16 into orow (skipped when orow is null: a row past
+// Nq), lse = (m + log2 l) * ln 2; g = 1, or 1 / (1 - p) for a dropout forward whose kept
+// weights entered u unscaled.  An empty row (l == 0) gives +0.0 and -inf.  Warp-collective.
 template <int DV>
 __device__ __forceinline__ void write_row(uint32_t taddr, float l_run, float m_run,
-                                          __nv_bfloat16 *orow, float *lse_out) {
+                                          __nv_bfloat16 *orow, float *lse_out, float gain = 1.f) {
     const bool empty = !(l_run > 0.f);
-    const float inv = empty ? 0.f : 1.f / l_run;
+    const float inv = empty ? 0.f : gain / l_run;
     uint4 *o4 = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
     for (int cc = 0; cc < DV / 32; ++cc) {
@@ -296,9 +297,9 @@ __device__ __forceinline__ void write_row(uint32_t taddr, float l_run, float m_r
 // different bank groups, so a warp's writes do not conflict.
 template <int DV>
 __device__ __forceinline__ void stage_row(uint32_t taddr, float l_run, float m_run, uint8_t *stage,
-                                          int r, float *lse_out) {
+                                          int r, float *lse_out, float gain = 1.f) {
     const bool empty = !(l_run > 0.f);
-    const float inv = empty ? 0.f : 1.f / l_run;
+    const float inv = empty ? 0.f : gain / l_run;
 #pragma unroll
     for (int cc = 0; cc < DV / 32; ++cc) {
         uint32_t ov[32];

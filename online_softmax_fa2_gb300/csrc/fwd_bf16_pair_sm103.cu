@@ -123,11 +123,12 @@ __device__ __forceinline__ Item next_item(const Args &a, const DropArgs &dr, int
 
 // Dropout (training forward): the 128 keep bits of a row for one key tile, as four 32-bit
 // words (bit t of word w = key 32w + t of the tile), applied to p after the row sum has taken
-// it: kept weights scaled by 1 / (1 - dropout_p), dropped ones 0.
-__device__ __forceinline__ void apply_keep(float (&x)[BK], const uint4 &keep, float inv_keep) {
+// it: dropped weights 0, kept ones as they are (the 1 / (1 - dropout_p) of the kept ones is
+// applied once, to the row's output, in the epilogue).
+__device__ __forceinline__ void apply_keep(float (&x)[BK], const uint4 &keep) {
     const uint32_t w[4] = {keep.x, keep.y, keep.z, keep.w};
 #pragma unroll
-    for (int k = 0; k < BK; ++k) x[k] = ((w[k >> 5] >> (k & 31)) & 1u) ? x[k] * inv_keep : 0.f;
+    for (int k = 0; k < BK; ++k) x[k] = ((w[k >> 5] >> (k & 31)) & 1u) ? x[k] : 0.f;
 }
 
 __device__ __forceinline__ uint4 ld_keep(const uint8_t *p) {
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float lsum = tile_exp<kBias>(x, c, m_run);
                 l_run = fmaf(alpha, l_run, lsum);
                 if constexpr (kDrop) {  // the row sum keeps the undropped weights
-                    apply_keep(x, keep, dr.inv_keep);
+                    apply_keep(x, keep);
                     if (keep_row && j + 1 < nX) keep = ld_keep(keep_row + (j + 1) * (BK / 8));
                 }
                 if (__any_sync(0xffffffffu, rescale)) scale_o<DV>(lane_addr + o_col, alpha);
@@ -509,12 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Q_B can load meanwhile; the store releases that slot.  With dv > dk the Q buffer
             // is too small and tile A writes its rows directly.
             if (!kStageA && X == 0) {
-                write_row<DV>(lane_addr + o_col, l_run, m_run, out_row(), out_lse());
+                write_row<DV>(lane_addr + o_col, l_run, m_run, out_row(), out_lse(), kDrop ? dr.inv_keep : 1.f);
                 ptx::tc_fence_before();
             } else {
                 const int sl = (g + it.nmax - 1) % VS;
                 uint8_t *stage = X ? smem + L::kVOff + sl * L::kVBytes : smem;
-                stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, out_lse());
+                stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, out_lse(), kDrop ? dr.inv_keep : 1.f);
                 ptx::tc_fence_before();
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&ctrl->o_staged[X]);
