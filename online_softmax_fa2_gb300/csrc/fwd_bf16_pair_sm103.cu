@@ -458,7 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_run = fmaf(alpha, l_run, lsum);
                 if constexpr (kDrop) {  // the row sum keeps the undropped weights
                     apply_keep(x, keep);
-                    if (keep_row && j + 1 < nX) keep = ld_keep(keep_row + (j + 1) * (BK / 8));
                 }
                 if (__any_sync(0xffffffffu, rescale)) scale_o<DV>(lane_addr + o_col, alpha);
                 // value rows past n inside this tile may hold anything: the warpgroup of the
@@ -477,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive(&ctrl->p_full[X]);
                 if (kBias && j + 1 < nX) load_bias(bias_row, bias_vec, kv0 + BK, it.n, x);
                 if constexpr (kDrop) {
+                    if (keep_row && j + 1 < nX) keep = ld_keep(keep_row + (j + 1) * (BK / 8));
                     if (dr.rng && i < a.Nq && j + 1 < nX)
                         keep = rng::keep128((uint32_t)i, (uint32_t)(kv0 + BK), bh, dr.offset, dr.seed_lo, dr.seed_hi,
                                             dr.p8x4);
