@@ -320,10 +320,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
 // With 2 to 8 query rows per sequence the per-key work grows with the rows while the bytes
 // read stay those of one row, so the scores and the value sums go to the tensor cores
 // (mma.sync m16n8k16, bf16 inputs, fp32 accumulation; the products are 16 keys by at most 8
-// rows, far below what tcgen05 tiles are for).  Each warp takes 16-key tiles of the split in
-// turn (tile w, w + 4, ...), copied into shared memory with cp.async (double-buffered, rows
-// padded to 16 B past 2*D so that ldmatrix reads are free of bank conflicts; keys past the
-// split are zero-filled, so nothing stored past kv_len reaches a product):
+// rows, far below what tcgen05 tiles are for).  Each warp owns one split of one (b, h): CTA x
+// of the grid holds splits 4x .. 4x + 3.  The warp walks its split's 16-key tiles, copied into
+// its own shared memory with cp.async (double-buffered, rows padded to 16 B past 2*D so that
+// ldmatrix reads are free of bank conflicts; keys past the split are zero-filled, so nothing
+// stored past kv_len reaches a product):
 //   S = Q K^T     M = 16 query rows (rows >= Nq are zero), N = 8 keys, K = 16 dims per step;
 //                 the K operand comes from ldmatrix on the [key][dim] tile;
 //   O^T += V^T P^T  M = 16 dims, N = 8 query rows, K = 16 keys; V^T comes from ldmatrix.trans,
@@ -331,8 +332,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecArgs a) {
 //                 g, keys 2t, 2t+1 of each 8-key half) is the fragment it must supply of P^T.
 // The online update runs per query row on the four lanes that hold it (row max over their
 // eight scores and two shuffles); the row's rescale factor reaches the lanes holding that row
-// of O^T by a shuffle.  At the end the four warps' states are merged in shared memory and the
-// split's state of each row is written as in the one-row kernel.
+// of O^T by a shuffle.  At the end the warp writes its split's state of each row straight
+// from its fragments, as the one-row kernel writes its split's: no state is merged across warps.
 
 constexpr int kRowsKT = 16;  // keys per warp tile
 constexpr int kRowsWarps = kThreads / 32;
@@ -342,8 +343,41 @@ struct RowsLayout {
     static constexpr int kRowBytes = 2 * D + 16;               // padded key row
     static constexpr int kTileBytes = kRowsKT * kRowBytes;     // one K or V tile
     static constexpr int kBytes = kRowsWarps * 2 * 2 * kTileBytes;  // [warp][stage][K, V]
-    static_assert(kRowsWarps * 8 * (2 + D) * 4 <= kBytes, "merge area");
 };
+
+// The fused merge for a warp that owns a whole split: lane 0 counts the split as done on the
+// (b, h) counter (tagged as in fused_tail); the warp whose count completes the S splits merges
+// every row.  Bounded like fused_tail.
+template <int D>
+__device__ __forceinline__ void fused_tail_warp(const DecArgs &a, int b, int h) {
+    __syncwarp();  // this warp's states are written (ordered before lane 0's fence below)
+    const int lane = threadIdx.x & 31;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();  // release: the states, visible device-wide before the count
+        unsigned long long *cnt = a.counters + (long long)b * a.H + h;
+        unsigned long long seen = *reinterpret_cast<volatile unsigned long long *>(cnt), mine = 0;
+        for (int tries = 0;; ++tries) {
+            mine = ((seen >> 16) == a.tag ? (seen & 0xffffull) : 0ull) + 1ull;
+            const unsigned long long prev = atomicCAS(cnt, seen, (a.tag << 16) | mine);
+            if (prev == seen) break;
+            seen = prev;
+            if (tries >= 4096) {
+                atomicOr(a.flags, kFlagWaitTimeout);
+                mine = 0;
+                break;
+            }
+        }
+        last = (mine == (unsigned long long)a.S);
+        if (last) __threadfence();  // acquire: the other splits' states, observed through their counts
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    for (int r = 0; r < a.Nq; ++r) {
+        const long long row = ((long long)b * a.H + h) * a.Nq + r;
+        merge_row<__nv_bfloat16>(a.part + row * a.S * (2 + D), a.S, 2 + D, D,
+                                 a.o + b * a.os0 + r * a.os1 + h * a.os2, a.lse ? a.lse + row : nullptr);
+    }
+}
 
 template <int D, bool kFuse>
 __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
@@ -352,17 +386,18 @@ __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int s = blockIdx.x * kRowsWarps + warp, h = blockIdx.y, b = blockIdx.z;
     const int nq = a.Nq;
     // launched as a programmatic dependent: global memory only after the previous kernel
     ptx::grid_dep_wait();
     ptx::launch_dependents();
+    if (s >= a.S) return;  // the last CTA's warps past the split count (no CTA-wide barrier below)
 
     int n = a.Nk;
     if (a.kv_lens) {
         int raw = a.kv_lens[b];
         n = min(max(raw, 0), a.Nk);
-        if (raw != n && threadIdx.x == 0 && s == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
+        if (raw != n && lane == 0 && s == 0 && h == 0) atomicOr(a.flags, kFlagKvLenClamped);
     }
     const int lo = (int)(((long long)s * n) / a.S), hi = (int)(((long long)(s + 1) * n) / a.S);
 
@@ -405,10 +440,10 @@ __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
     };
     const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
     int st = 0;
-    if (warp < ntiles) issue(warp, 0);
+    if (ntiles > 0) issue(0, 0);
     else cp_async_commit();
-    for (int T = warp; T < ntiles; T += kRowsWarps, st ^= 1) {
-        if (T + kRowsWarps < ntiles) issue(T + kRowsWarps, st ^ 1);
+    for (int T = 0; T < ntiles; ++T, st ^= 1) {
+        if (T + 1 < ntiles) issue(T + 1, st ^ 1);
         else cp_async_commit();
         cp_async_wait<1>();
         __syncwarp();
@@ -468,58 +503,31 @@ __global__ void __launch_bounds__(kThreads) decode_rows_mma_kernel(DecArgs a) {
     cp_async_wait<0>();
     l_g += __shfl_xor_sync(0xffffffffu, l_g, 1);
     l_g += __shfl_xor_sync(0xffffffffu, l_g, 2);
-    __syncthreads();  // the tiles are no longer read: their space holds the warps' states
 
-    float *sm_m = reinterpret_cast<float *>(dsm);        // [warp][8 rows]
-    float *sm_l = sm_m + kRowsWarps * 8;                 // [warp][8 rows]
-    float *sm_o = sm_l + kRowsWarps * 8;                 // [warp][8 rows][D]
-    if (t == 0) {
-        sm_m[warp * 8 + g] = m_g;
-        sm_l[warp * 8 + g] = l_g;
+    // the split's state of each row: (m, l) from the lanes that own the row (t == 0), u from the
+    // fragments of O^T (lane (g, t) holds dims 16 mt + g (+ 8) of rows 2t and 2t + 1); a row
+    // that saw no key of the split gets (-inf, 0, 0)
+    float *part_b = a.part + (((long long)b * a.H + h) * nq) * a.S * (2 + D);
+    auto state = [&](int r) { return part_b + ((long long)r * a.S + s) * (2 + D); };
+    if (t == 0 && g < nq) {
+        float *out = state(g);
+        out[0] = l_g > 0.f ? m_g * kLn2 : -INFINITY;
+        out[1] = l_g;
     }
 #pragma unroll
     for (int mt = 0; mt < NK; ++mt) {
-        float *r0 = sm_o + (warp * 8 + 2 * t) * D + 16 * mt + g;
-        float *r1 = r0 + D;
-        r0[0] = o[mt][0];
-        r1[0] = o[mt][1];
-        r0[8] = o[mt][2];
-        r1[8] = o[mt][3];
-    }
-    __syncthreads();
-
-    // thread c owns column c of every row
-    for (int r = 0; r < nq; ++r) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kRowsWarps; ++w)
-            if (sm_l[w * 8 + r] > 0.f) M = fmaxf(M, sm_m[w * 8 + r]);
-        float *out = a.part + ((((long long)b * a.H + h) * nq + r) * a.S + s) * (2 + D);
-        if (M == -INFINITY) {  // empty split
-            for (int c = threadIdx.x; c < D; c += kThreads) out[2 + c] = 0.f;
-            if (threadIdx.x == 0) {
-                out[0] = -INFINITY;
-                out[1] = 0.f;
-            }
-            continue;
+        if (2 * t < nq) {
+            float *r0 = state(2 * t) + 2 + 16 * mt + g;
+            r0[0] = o[mt][0];
+            r0[8] = o[mt][2];
         }
-        float Lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kRowsWarps; ++w)
-            if (sm_l[w * 8 + r] > 0.f) Lsum = fmaf(ex2(sm_m[w * 8 + r] - M), sm_l[w * 8 + r], Lsum);
-        for (int c = threadIdx.x; c < D; c += kThreads) {
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kRowsWarps; ++w)
-                if (sm_l[w * 8 + r] > 0.f) acc = fmaf(ex2(sm_m[w * 8 + r] - M), sm_o[(w * 8 + r) * D + c], acc);
-            out[2 + c] = acc;
-        }
-        if (threadIdx.x == 0) {
-            out[0] = M * kLn2;
-            out[1] = Lsum;
+        if (2 * t + 1 < nq) {
+            float *r1 = state(2 * t + 1) + 2 + 16 * mt + g;
+            r1[0] = o[mt][1];
+            r1[8] = o[mt][3];
         }
     }
-    if constexpr (kFuse) fused_tail<D>(a, b, h);
+    if constexpr (kFuse) fused_tail_warp<D>(a, b, h);
 }
 
 // Merge: one warp per (b, h, query row i) -- row r = (b*H + h)*Nq + i, whose state s sits at
@@ -580,10 +588,11 @@ attn_status_t launch_decode_split(const attn_fwd_params_t &p, int num_splits, fl
         auto kern = p.dk == 64 ? (fuse ? decode_split_kernel<64, true> : decode_split_kernel<64, false>)
                                : (fuse ? decode_split_kernel<128, true> : decode_split_kernel<128, false>);
         e = launch_pdl(kern, grid, dim3(kThreads), 0, st, a);
-    } else if (p.dk == 64) {
-        e = fuse ? launch_rows<64, true>(a, grid, st) : launch_rows<64, false>(a, grid, st);
     } else {
-        e = fuse ? launch_rows<128, true>(a, grid, st) : launch_rows<128, false>(a, grid, st);
+        // several rows: one warp per split, kRowsWarps splits per CTA
+        const dim3 rgrid((unsigned)((num_splits + kRowsWarps - 1) / kRowsWarps), (unsigned)p.H, (unsigned)p.B);
+        if (p.dk == 64) e = fuse ? launch_rows<64, true>(a, rgrid, st) : launch_rows<64, false>(a, rgrid, st);
+        else e = fuse ? launch_rows<128, true>(a, rgrid, st) : launch_rows<128, false>(a, rgrid, st);
     }
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode rows launch: %s", cudaGetErrorString(e));
     e = cudaGetLastError();
