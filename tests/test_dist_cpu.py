@@ -38,7 +38,7 @@ def _worker(rank, world, port, queue):
         rate = bench.job_rate(w, 2.0e12, slowest)  # 2 TFLOP per rank per step
         out = io.StringIO()
         with contextlib.redirect_stdout(out):
-            rc = bench.run_reference(argparse.Namespace(steps=1, warmup=0))
+            rc = bench.run_reference(argparse.Namespace(steps=1, warmup=0, ref_seconds=0.0))
         queue.put((r, w, slowest, rate, rc, out.getvalue()))
         dist.barrier()
     finally:
