@@ -109,8 +109,7 @@ typedef enum {
  *                       disables dropout and asks exactly that of a training backward).
  *                       bfloat16: dk <= 128 only, the mask 16-byte aligned with strides that
  *                       are multiples of 16 bytes.  Not taken by attn_decode_splitkv, nor by
- *                       attn_bwd other than for dk = dv = 128 without a bias
- *                       (ATTN_ERR_UNSUPPORTED).
+ *                       attn_bwd together with a bias (ATTN_ERR_UNSUPPORTED).
  *   dropout_p           in [0, 1) with a mask or with dropout_rng = 1; must be 0 otherwise.
  *   dropout_rng         0: the keep decisions come from dropout_mask (or there is no dropout).
  *                       1: they are drawn in-kernel, and no mask is read or stored anywhere:
@@ -348,12 +347,11 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t dk);
  * The mask, bias, kv_lens, causal and dropout settings must be the forward's: with a
  * dropout_mask in fwd (the forward's keep bits and dropout_p) the gradient reaching the
  * weights carries the mask and the 1 / (1 - p) scale, dV is formed from the kept, scaled
- * weights, and c_i = g_i . o_i already holds the dropout through o (dk = dv = 128 without a
- * bias only; otherwise ATTN_ERR_UNSUPPORTED).  The bias is fixed: no gradient is formed for it.  An empty row (lse = -inf) passes no gradient, and a key that no
+ * weights, and c_i = g_i . o_i already holds the dropout through o (without a bias only;
+ * with one ATTN_ERR_UNSUPPORTED).  The bias is fixed: no gradient is formed for it.  An empty row (lse = -inf) passes no gradient, and a key that no
  * row sees gets dK = dV = 0.
  * Queues three kernels on `stream`: the row terms, the products (on the 5th-generation
- * tensor cores for dk = dv = 128 without a bias, on warp-level tensor-core tiles otherwise),
- * and the conversion of dQ to bf16.  Supported: bfloat16, dk == dv in {64, 128}; every tensor
+ * tensor cores), and the conversion of dQ to bf16.  Supported: bfloat16, dk == dv in {64, 128}; every tensor
  * 16-byte aligned with strides that are multiples of 8 elements.  The workspace is
  * caller-owned device memory of at least attn_bwd_workspace_bytes(B, H, Nq, dk) bytes,
  * 16-byte aligned; its contents on entry do not matter.  dQ is accumulated with atomic

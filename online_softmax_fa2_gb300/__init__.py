@@ -379,7 +379,7 @@ def attn_bwd(q, k, v, o, lse, dout, bias=None, kv_lens=None, causal=False, scale
              dropout_seed=None, dropout_offset=0):
     """Gradients (dq, dk, dv) of a loss through o = attn_fwd(q, k, v, ...), given dout = dL/do
     and the forward's o and lse (bfloat16, dk == dv in {64, 128}).  The mask, bias, kv_lens,
-    causal and dropout settings must be the forward's (dropout: dk = dv = 128 without a bias);
+    causal and dropout settings must be the forward's (dropout: without a bias);
     the bias gets no gradient."""
     lib = load()
     B, Nq, H, d = q.shape

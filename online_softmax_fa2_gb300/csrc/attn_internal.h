@@ -49,7 +49,7 @@ attn_status_t launch_bwd(const attn_bwd_params_t &p, float *dq_acc, float *crow,
 attn_status_t encode(CUtensorMap *m, const void *ptr, int64_t B, int64_t N, int64_t H, int64_t d,
                      const int64_t s[3], const char *name);
 
-// Backward of dk == dv == 128 without a bias on the tcgen05 tensor cores (bwd_tc_sm103.cu);
+// The backward's products on the tcgen05 tensor cores (bwd_tc_sm103.cu; dk == dv in {64, 128});
 // dq_acc, crow and lrow (lse * log2 e, rows padded to a multiple of 128) as for launch_bwd,
 // already filled by the prep kernel.
 attn_status_t launch_bwd_tc(const attn_bwd_params_t &p, float *dq_acc, const float *crow, const float *lrow,

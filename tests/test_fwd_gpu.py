@@ -181,6 +181,23 @@ def test_bf16_masked_positions_bit_exact():
     compare(o2, l2, o_ref, l_ref, torch.bfloat16, what="poisoned")
 
 
+@pytest.mark.parametrize("dk,dv,causal", [(128, 128, True), (128, 64, False), (64, 64, True), (64, 128, True)])
+def test_bf16_staged_bias_at_dk_up_to_128(dk, dv, causal):
+    # bias rows 16-byte aligned (Nk a multiple of 4): with dk >= dv the bias is staged by TMA in
+    # the one-tile kernel, with dk < dv it is read into registers by the two-tile kernel; NaN
+    # stored at every masked position must change no output bit either way
+    kw = dict(B=3, H=2, Nq=300, Nk=336, dk=dk, dv=dv, dtype=torch.bfloat16, causal=causal, bias=True,
+              kv_lens=[336, 150, 77], seed=31, device=DEV, bias_mask_p=0.05)
+    clean = wl.make_prefill(**kw, poison=False)
+    dirty = wl.make_prefill(**kw, poison=True)
+    o1, l1 = run(clean)
+    o2, l2 = run(dirty)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+    o_ref, l_ref, _ = oracle_full(clean)
+    compare(o2, l2, o_ref, l_ref, torch.bfloat16, empty=empty_rows(clean), what=f"staged bias {dk}/{dv}")
+
+
 def test_bf16_empty_cases():
     # no keys at all
     a = wl.make_prefill(2, 2, 130, 0, 128, 128, torch.bfloat16, seed=25, device=DEV)
