@@ -37,9 +37,12 @@ def sequence_parallel_attn(q, k_shard, v_shard, key_offset, nk_total, group=None
 
     B, Nq, H, _ = q.shape
     dv = v_shard.shape[3]
-    part = ofa.attn_fwd_partial(q, k_shard, v_shard, key_offset, nk_total, kv_lens=kv_lens, bias=bias,
-                                causal=causal, scale=scale, stream=stream)
-    allp = gather_states(part, group)
-    world = allp.shape[0]
-    return ofa.attn_merge_states_rows(allp, B, H, Nq, dv, world, row_stride=2 + dv,
-                                      split_stride=part.numel(), dtype=q.dtype, stream=stream)
+    s = torch.cuda.current_stream(q.device) if stream is None else stream
+    # the partial kernel, the collective and the merge run in that order on one stream
+    with torch.cuda.stream(s):
+        part = ofa.attn_fwd_partial(q, k_shard, v_shard, key_offset, nk_total, kv_lens=kv_lens, bias=bias,
+                                    causal=causal, scale=scale, stream=s)
+        allp = gather_states(part, group)
+        world = allp.shape[0]
+        return ofa.attn_merge_states_rows(allp, B, H, Nq, dv, world, row_stride=2 + dv,
+                                          split_stride=part.numel(), dtype=q.dtype, stream=s)

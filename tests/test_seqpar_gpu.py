@@ -124,3 +124,35 @@ def test_causal_b4_h16_n2048_d128_two_shards_sampled_heads():
         o_ref, l_ref, _ = oracle.attn_fwd(sub(a.q), sub(a.k), sub(a.v), causal=True, scale=a.scale)
         assert np.max(np.abs(o[b:b + 1, :, h:h + 1].float().cpu().numpy() - o_ref)) <= TOL[torch.bfloat16]["o"]
         assert np.max(np.abs(lse[b, h].cpu().numpy() - l_ref[0, 0])) <= TOL[torch.bfloat16]["lse"]
+
+
+def test_sequence_parallel_attn_on_a_one_rank_nccl_group():
+    # the whole path of seqpar.sequence_parallel_attn (partial kernel, NCCL all-gather, merge)
+    # on a one-rank group holding every key, on a side stream: it must give attn_fwd's bits
+    import socket
+    import torch.distributed as dist
+    from online_softmax_fa2_gb300 import seqpar
+
+    a = wl.make_prefill(2, 3, 300, 333, 128, 128, torch.bfloat16, causal=True, kv_lens=[333, 100],
+                        seed=81, device=DEV)
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        o, lse = seqpar.sequence_parallel_attn(a.q, a.k, a.v, 0, a.Nk, kv_lens=a.kv_lens, causal=True,
+                                               scale=a.scale, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    allp = shard_states(a, [0, a.Nk])
+    o2, l2 = merge(a, allp)
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse, l2)
+    o_ref, l_ref, _ = oracle.attn_fwd(cpu32(a.q), cpu32(a.k), cpu32(a.v), kv_lens=a.kv_lens.cpu(), causal=True,
+                                      scale=a.scale)
+    compare(o, lse, o_ref, l_ref, torch.bfloat16, empty=empty_rows(a), what="seqpar one rank")
