@@ -404,15 +404,16 @@ def run_reference(args):
 
 
 def prefill_object(ofa, a, args, stream, pk, pk_kind, clk_windows, barrier, world, dev, n_sets,
-                   roof_kind, traffic):
+                   roof_kind, traffic, **fwd_kwargs):
     """Time one forward workload (rotated input copies, back-to-back steps) and describe it:
     value, time per step and roofline ("tensor", or "combined": max(FLOPs / tensor peak,
-    algorithmic bytes / HBM peak))."""
+    algorithmic bytes / HBM peak)).  fwd_kwargs go to every attn_fwd call (dropout)."""
     sets = rotated_inputs(a, n_sets)
 
     def step(n):
         q, k, v, b, o, lse = sets[n % n_sets]
-        ofa.attn_fwd(q, k, v, bias=b, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale, out=o, lse=lse)
+        ofa.attn_fwd(q, k, v, bias=b, kv_lens=a.kv_lens, causal=a.causal, scale=a.scale, out=o, lse=lse,
+                     **fwd_kwargs)
 
     est = warm(step, max(3, args.warmup), stream)
     ofa.device_error_flags()
@@ -573,6 +574,17 @@ def run_ours(args):
             extra["padbias"]["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": threads,
                                                 "kind": "oracle", "sample": desc, "seconds": secs}
         del pb
+        # the headline workload with dropout p = 0.1: keep decisions drawn in-kernel, and read
+        # from a bit-packed keep mask (33.5 MB, one per step here)
+        dr = wl.causal_2k(dev)
+        keep_mask = wl.pack_keep_mask(wl.dropout_keep(dr.B, dr.H, dr.Nq, dr.Nk, 0.1, seed=1, device=dev))
+        extra["dropout"] = {
+            "in_kernel_draws": prefill_object(ofa, dr, args, stream, pk, pk_kind, other_windows, barrier, world,
+                                              dev, 4, "tensor", None, dropout_p=0.1, dropout_seed=1),
+            "keep_mask": prefill_object(ofa, dr, args, stream, pk, pk_kind, other_windows, barrier, world, dev,
+                                        4, "tensor", None, dropout_mask=keep_mask, dropout_p=0.1),
+            "p": 0.1}
+        del dr, keep_mask
 
     # ---------------------------------------------------------------- split-KV decode (HBM)
     dec = None
@@ -611,6 +623,22 @@ def run_ours(args):
         ms_d, reps = time_steps(dstep, args.steps, stream, args.min_seconds, est, barrier, other_windows)
         ms_d = max_over_ranks(ms_d, world, dev)
         ms_f = max_over_ranks(ms_f, world, dev)
+        del ws, wsf, od, ld
+        # four query rows per sequence (bottom-right causal) against the same cache
+        d4 = wl.decode(dev, nq=4, causal=True)
+        ws4 = torch.empty(ofa.decode_workspace_bytes(d4.B, d4.H, d4.dv, d4.num_splits, 4) // 4,
+                          dtype=torch.float32, device=dev)
+        o4 = torch.empty((d4.B, 4, d4.H, d4.dv), dtype=d4.q.dtype, device=dev)
+        l4 = torch.empty((d4.B, d4.H, 4), dtype=torch.float32, device=dev)
+
+        def dstep4(n):
+            ofa.attn_decode_splitkv(d4.q, d4.k, d4.v, kv_lens=d4.kv_lens, num_splits=d4.num_splits,
+                                    scale=d4.scale, workspace=ws4, out=o4, lse=l4, causal=True)
+
+        est = warm(dstep4, max(3, args.warmup), stream)
+        ms_4, reps4 = time_steps(dstep4, args.steps, stream, args.min_seconds / 2, est, barrier, other_windows)
+        ms_4 = max_over_ranks(ms_4, world, dev)
+        del d4, ws4, o4, l4
         gbs = job_rate(1, d.kv_bytes(), ms_d, 1e9)  # one GPU's rate, against one GPU's peak
         dec = {"workload": "bf16_decode_b64_h32_l8192_d128_splits16",
                "value": job_rate(world, d.kv_bytes(), ms_d, 1e9),
@@ -628,54 +656,78 @@ def run_ours(args):
                             "traffic": profiled_traffic("decode_split_kernel.decode_b64_h32_l8192_d128.md",
                                                         ("decode.cu", "sm100_ptx.cuh", "warp_mma.cuh",
                                                          "attn_internal.h"))}}
-        del d, ws, wsf
+        g4 = job_rate(1, d.kv_bytes(), ms_4, 1e9)
+        dec["rows4"] = {"workload": "bf16_decode_b64_h32_l8192_d128_nq4_causal_splits16",
+                        "value": job_rate(world, d.kv_bytes(), ms_4, 1e9), "unit": "GB/s", "ms_per_step": ms_4,
+                        "repeats": reps4, "path": "attn_decode_splitkv, 4 query rows per sequence (decode_rows_mma_kernel + merge)",
+                        "roofline": {"bound": "hbm", "achieved": g4, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                     "frac": g4 / pk["hbm_gbs"], "peak_kind": f"{pk_kind} copy bandwidth (read + write)"}}
+        del d
 
     # backward of the same workload (dQ, dK, dV from o, lse and a seeded random dO): reported
     # beside the forward's line with its own tensor roofline, taken over the whole backward
     # step (row terms, products, dQ conversion: three launches)
     bwd = None
     if not args.no_backward:
-        # three copies of the step's inputs (q, k, v, o, lse, dO) with gradients of their own
-        # (about 400 MB, over three times L2), stepped back to back like the forward
-        o_b, l_b = ofa.attn_fwd(a.q, a.k, a.v, causal=True, scale=a.scale)
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(7)
-        dout_b = torch.randn(o_b.shape, generator=gen, device=dev).to(o_b.dtype)
-        ws_b = torch.empty(ofa.bwd_workspace_bytes(a.B, a.H, a.Nq, a.dk) // 4 + 4, dtype=torch.float32,
-                           device=dev)
-        n_bsets = 3
-        bsets = []
-        for t in range(n_bsets):
-            cp = (lambda x: x if t == 0 else x.clone())
-            bsets.append((cp(a.q), cp(a.k), cp(a.v), cp(o_b), cp(l_b), cp(dout_b),
-                          torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)))
+        def backward_ms(wa, **drop):
+            """Time the backward of workload wa (dQ, dK, dV from o, lse and a seeded random dO)
+            over three input copies with gradients of their own, stepped back to back like the
+            forward; drop: the forward's dropout settings, passed again."""
+            o_b, l_b = ofa.attn_fwd(wa.q, wa.k, wa.v, bias=wa.bias, causal=wa.causal, scale=wa.scale, **drop)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(7)
+            dout_b = torch.randn(o_b.shape, generator=gen, device=dev).to(o_b.dtype)
+            ws_b = torch.empty(ofa.bwd_workspace_bytes(wa.B, wa.H, wa.Nq, wa.dk) // 4 + 4, dtype=torch.float32,
+                               device=dev)
+            bsets = []
+            for t in range(3):
+                cp = (lambda x: x if (t == 0 or x is None) else x.clone())
+                bsets.append((cp(wa.q), cp(wa.k), cp(wa.v), cp(wa.bias), cp(o_b), cp(l_b), cp(dout_b),
+                              torch.empty_like(wa.q), torch.empty_like(wa.k), torch.empty_like(wa.v)))
 
-        def bstep(n):
-            q_, k_, v_, o_, l_, g_, dq_, dk_, dv_ = bsets[n % n_bsets]
-            ofa.attn_bwd(q_, k_, v_, o_, l_, g_, causal=True, scale=a.scale, dq=dq_, dk=dk_, dv=dv_,
-                         workspace=ws_b)
+            def bstep(n):
+                q_, k_, v_, b_, o_, l_, g_, dq_, dk_, dv_ = bsets[n % 3]
+                ofa.attn_bwd(q_, k_, v_, o_, l_, g_, bias=b_, causal=wa.causal, scale=wa.scale, dq=dq_, dk=dk_,
+                             dv=dv_, workspace=ws_b, **drop)
 
-        est_b = warm(bstep, max(3, args.warmup), stream)
-        ofa.device_error_flags()
-        ms_b, reps_b = time_steps(bstep, args.steps, stream, args.min_seconds, est_b, barrier, other_windows)
-        if ofa.device_error_flags() & 1:
-            raise RuntimeError("a backward kernel gave up a bounded wait during the timed region")
-        ms_b = max_over_ranks(ms_b, world, dev)
-        bflops = a.visible_pairs() * (6 * a.dk + 4 * a.dv)   # five products per visible pair
-        tb = job_rate(1, bflops, ms_b)
-        bwd = {"workload": "bf16_causal_b4_h16_n2048_d128_backward", "value": job_rate(world, bflops, ms_b),
-               "unit": "TFLOP/s", "ms_per_step": ms_b, "steps": args.steps, "repeats": reps_b,
-               "flops_per_step": bflops, "gpu_launches_per_step": 3,
-               "l2": f"inputs rotated over {n_bsets} copies (about 400 MB > 129 MB L2), no flush",
-               "roofline": {"bound": "tensor", "achieved": tb, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                            "frac": tb / pk["bf16_tflops"], "peak_kind": f"{pk_kind} dense bf16 (burst)",
-                            "frac_nominal": tb / NOMINAL["bf16_tflops"],
-                            "over": "the whole backward step (bwd_prep_kernel, bwd_tc_kernel, bwd_dq_kernel)",
-                            "traffic": profiled_traffic("bwd_tc_kernel.causal_b4_h16_n2048_d128.md",
-                                                        ("bwd_tc_sm103.cu", "sm100_ptx.cuh", "fwd_bf16_common.cuh",
-                                                         "dropout_rng.cuh", "attn_internal.h")),
-                            "traffic_kernel": "bwd_tc_kernel (its DRAM bytes per launch)"}}
-        del o_b, l_b, dout_b, ws_b, bsets
+            est_b = warm(bstep, max(3, args.warmup), stream)
+            ofa.device_error_flags()
+            ms_b, reps_b = time_steps(bstep, args.steps, stream, args.min_seconds / (1 if not drop and wa is a else 2),
+                                      est_b, barrier, other_windows)
+            if ofa.device_error_flags() & 1:
+                raise RuntimeError("a backward kernel gave up a bounded wait during the timed region")
+            return max_over_ranks(ms_b, world, dev), reps_b
+
+        def backward_obj(wa, ms_b, reps_b, name):
+            bflops = wa.visible_pairs() * (6 * wa.dk + 4 * wa.dv)   # five products per visible pair
+            tb = job_rate(1, bflops, ms_b)
+            return {"workload": name, "value": job_rate(world, bflops, ms_b), "unit": "TFLOP/s",
+                    "ms_per_step": ms_b, "steps": args.steps, "repeats": reps_b, "flops_per_step": bflops,
+                    "gpu_launches_per_step": 3,
+                    "l2": "inputs rotated over 3 copies (more than 129 MB L2), no flush",
+                    "roofline": {"bound": "tensor", "achieved": tb, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                 "frac": tb / pk["bf16_tflops"], "peak_kind": f"{pk_kind} dense bf16 (burst)",
+                                 "frac_nominal": tb / NOMINAL["bf16_tflops"],
+                                 "over": "the whole backward step (bwd_prep_kernel, bwd_tc_kernel, bwd_dq_kernel)"}}
+
+        ms_b, reps_b = backward_ms(a)
+        bwd = backward_obj(a, ms_b, reps_b, "bf16_causal_b4_h16_n2048_d128_backward")
+        bwd["roofline"]["traffic"] = profiled_traffic("bwd_tc_kernel.causal_b4_h16_n2048_d128.md",
+                                                      ("bwd_tc_sm103.cu", "sm100_ptx.cuh", "fwd_bf16_common.cuh",
+                                                       "dropout_rng.cuh", "attn_internal.h"))
+        bwd["roofline"]["traffic_kernel"] = "bwd_tc_kernel (its DRAM bytes per launch)"
+        if not args.no_extra:
+            # the same backward with dropout p = 0.1 drawn in-kernel; at d = 64; with an fp32 bias
+            ms_x, reps_x = backward_ms(a, dropout_p=0.1, dropout_seed=1)
+            bwd["dropout_in_kernel_draws"] = backward_obj(a, ms_x, reps_x, "bf16_causal_b4_h16_n2048_d128_backward_dropout0.1")
+            a64 = wl.causal_2k(dev, d=64)
+            ms_x, reps_x = backward_ms(a64)
+            bwd["d64"] = backward_obj(a64, ms_x, reps_x, a64.name + "_backward")
+            del a64
+            ab = wl.causal_2k(dev, bias=True, B=2, H=8)
+            ms_x, reps_x = backward_ms(ab)
+            bwd["bias"] = backward_obj(ab, ms_x, reps_x, ab.name + "_backward")
+            del ab
 
     clocks = clk.stop(windows)
     clk_all = None
