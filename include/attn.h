@@ -242,8 +242,7 @@ attn_status_t attn_decode_splitkv_fused(const attn_fwd_params_t *params, int32_t
  *     limit: a bad argument returns its own status, not ATTN_ERR_WORKSPACE.
  *   - The first call from a CUDA context looks up the array's device address (with the
  *     device current) and caches it per device, together with that context's unique id; a
- *     call from a new context (e.g. after cudaDeviceReset) looks it up again.  Make the first
- *     call on a device, and the first after a reset, before any stream capture.
+ *     call from a new context (e.g. after cudaDeviceReset) looks it up again.
  *   - All calls share the one array.  Every call writes each partial state it reads, so
  *     nothing needs clearing, but calls whose work overlaps on the GPU (different streams,
  *     several host threads) race on it: order them on one stream.

@@ -356,8 +356,8 @@ def attn_decode_splitkv_noalloc(q, k, v, kv_lens=None, num_splits=16, bias=None,
     """Split-KV decode that allocates no device memory in the library: for callers that
     cannot allocate while decoding.  The partial states go to a 32 MiB device array built
     into the library (shared by every call: order calls on one stream).  The first call from a
-    CUDA context looks up that array's address; make it before any stream capture.  Returns
-    (o, lse); o and lse are allocated here only when not passed in."""
+    CUDA context looks up that array's address.  Returns (o, lse); o and lse are allocated here
+    only when not passed in."""
     lib = load()
     B, Nq, H, _ = q.shape
     dv = v.shape[3]
