@@ -299,59 +299,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BQ, BK, false);
             constexpr uint32_t kIdO = ptx::idesc_bf16_f32(BQ, DV, true);
-            const uint32_t q_addr = ptx::smem_u32(smem);
+            // The tensor cores' queue holds little more than one product, so whatever this
+            // thread does between two groups of products leaves them idle for about as long.
+            // It therefore keeps everything ready: ring slots and barrier parities advance by
+            // one step per key tile (no division), and shared-memory descriptors are kept as
+            // their 32-bit low words (ptx::mma_ss_lo), stepped by adds.
+            const uint32_t q_lo = ptx::sdesc_lo(ptx::smem_u32(smem), 16);  // Q_A; K-major: LBO 16 B
+            // K slot s: q_lo + kKLo + s * kKStep; V slot s (MN-major, LBO = one panel): likewise
+            constexpr uint32_t kKLo = L::kKOff >> 4, kKStep = L::kKBytes >> 4, kVStep = L::kVBytes >> 4;
+            constexpr uint32_t kVLo = (L::kVOff >> 4) + (((uint32_t)kPanelBytes >> 4) << 16) - (1u << 16);
             auto wait = [&](uint64_t *bar, uint32_t parity) {
                 return ptx::mbar_wait(bar, parity, abort, a.flags, kFlagWaitTimeout, kWaitLimitNs);
             };
-            // S_t = Q_t K^T of key tile gj (ring numbering) into TMEM columns [t*128, t*128 + 128)
-            auto issue_s = [&](int t, int gj) -> bool {
-                const int ks = gj % KS;
-                if (!wait(&ctrl->k_full[ks], (gj / KS) & 1)) return false;
-                ptx::tc_fence_after();
-                uint32_t k_addr = ptx::smem_u32(smem + L::kKOff + ks * L::kKBytes);
-                uint32_t qa = q_addr + t * L::kQBytes;
-                ptx::opaque(qa);  // rebuilt per call: the issuer keeps no descriptors live
-                // successive K-steps differ only in the start address (bits 0-13, 16-byte units;
-                // shared-memory addresses stay below 2^18, so the field never carries)
-                const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024), kd = ptx::sdesc_sw128(k_addr, 16, 1024);
+            // S_t = Q_t K^T into TMEM columns [t*128, t*128 + 128), K in ring slot ks
+            // (the bases are hidden from the optimiser so that the per-step operands are formed by
+            // one add each instead of being hoisted out of the loops into registers)
+            auto s_products = [&](int t, int ks) {
+                uint32_t ql = q_lo, tm = tmem;
+                ptx::opaque(ql);
+                ptx::opaque(tm);
+                const uint32_t qt = ql + t * (L::kQBytes >> 4), kt = ql + kKLo + ks * kKStep;
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
-                    ptx::mma_ss(tmem + t * BQ, qd + off, kd + off, kIdS, kk > 0 ? 1u : 0u);
+                    ptx::mma_ss_lo(tm + t * BQ, qt + off, kt + off, kIdS, kk > 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(&ctrl->s_full[t]);
-                return true;
             };
-            // O_t += P_t V_j, then S_t(j+1) into the columns P_t(j) occupies: tcgen05.mma
-            // operations issued by one thread execute in issue order, so the product has read
-            // P_t(j) before S_t(j+1) is written; and the commit behind s_full[t] covers that
-            // product, so O_t is complete when the softmax sees S_t(j+1).
-            auto step = [&](int t, int nt, int ut, int j, int gj, int vs) -> bool {
-                if (!wait(&ctrl->p_full[t], (ut + j) & 1) || !wait(&ctrl->v_full[vs], (gj / VS) & 1))
-                    return false;
-                ptx::tc_fence_after();
-                const uint64_t vd = ptx::sdesc_sw128(ptx::smem_u32(smem + L::kVOff + vs * L::kVBytes),
-                                                     kPanelBytes, 1024);
+            // O_t (+)= P_t V, P_t from TMEM columns [t*128, t*128 + 64), V in ring slot vs
+            auto pv_products = [&](int t, int vs, bool first) {
+                uint32_t ql = q_lo, tm = tmem;
+                ptx::opaque(ql);
+                ptx::opaque(tm);
+                const uint32_t vt = ql + kVLo + vs * kVStep;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    ptx::mma_ts(tmem + 2 * BQ + t * BQ, tmem + t * BQ + kk * 8, vd + ((kk * 16 * 128) >> 4),
-                                kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == nt - 1) ptx::mma_commit(&ctrl->o_final[t]);
-                if (j + 1 < nt) {
-                    if (!issue_s(t, gj + 1)) return false;
-                    if (j + 2 == nt) ptx::mma_commit(&ctrl->q_empty[t]);  // last S_t has read Q_t
-                }
-                return true;
+                    ptx::mma_ts_lo(tm + 2 * BQ + t * BQ, tm + t * BQ + kk * 8, vt + ((kk * 16 * 128) >> 4), kIdO,
+                                   (!first || kk > 0) ? 1u : 0u);
             };
-            // first S of a tile: the previous item's last P V product of that tile, issued
-            // earlier, reads its P from these columns first (issue order)
-            auto first_s = [&](int t, int nt, int &nq, int g0) -> bool {
-                if (!wait(&ctrl->q_full[t], nq & 1) || !issue_s(t, g0)) return false;
-                ++nq;
-                if (nt == 1) ptx::mma_commit(&ctrl->q_empty[t]);
-                return true;
-            };
-            int g = 0, nqA = 0, nqB = 0, uA = 0, uB = 0;
+            // ring slots of the next K tile and of the current V tile; barrier parities as bits:
+            // 0 K full, 1 V full, 2/3 Q_A/Q_B full, 4/5 P_A/P_B handed over
+            int ks = 0, vs = 0;
+            uint32_t ph = 0;
+            auto par = [&](int bit) -> uint32_t { return (ph >> bit) & 1u; };
+            auto flip = [&](int bit) { ph ^= 1u << bit; };
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int k = item_index(r, cta, G);
@@ -359,25 +350,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item it = decode_item<kPartial>(a, dr, k, false);
                 if (it.nmax == 0) continue;
                 const int nA = it.nA, nB = it.nB, nmax = it.nmax;
-                if (nA > 0 && !first_s(0, nA, nqA, g)) break;
-                if (nB > 0 && !first_s(1, nB, nqB, g)) break;
-                ptx::mma_commit(&ctrl->k_empty[g % KS]);
+                // first S of each tile: the previous item's last P V product of that tile, issued
+                // earlier, reads its P from these columns first (issue order)
+                if (!wait(&ctrl->k_full[ks], par(0))) break;
+                if (nA > 0) {
+                    if (!wait(&ctrl->q_full[0], par(2))) break;
+                    flip(2);
+                    ptx::tc_fence_after();
+                    s_products(0, ks);
+                    if (nA == 1) ptx::mma_commit(&ctrl->q_empty[0]);
+                }
+                if (nB > 0) {
+                    if (!wait(&ctrl->q_full[1], par(3))) break;
+                    flip(3);
+                    ptx::tc_fence_after();
+                    s_products(1, ks);
+                    if (nB == 1) ptx::mma_commit(&ctrl->q_empty[1]);
+                }
+                ptx::mma_commit(&ctrl->k_empty[ks]);
+                if (++ks == KS) { ks = 0; flip(0); }
                 for (int j = 0; j < nmax; ++j) {
-                    const int gj = g + j, vs = gj % VS;
-                    if ((j < nA && !step(0, nA, uA, j, gj, vs)) || (j < nB && !step(1, nB, uB, j, gj, vs))) {
+                    // O_t += P_t V_j, then S_t(j+1) into the columns P_t(j) occupies:
+                    // tcgen05.mma operations issued by one thread execute in issue order, so
+                    // the product has read P_t(j) before S_t(j+1) is written; and the commit
+                    // behind s_full[t] covers that product, so O_t is complete when the
+                    // softmax sees S_t(j+1).
+                    const bool more = j + 1 < nmax;
+                    if (!wait(&ctrl->v_full[vs], par(1)) || (more && !wait(&ctrl->k_full[ks], par(0)))) {
                         ok = false;
                         break;
                     }
+                    if (j < nA) {
+                        if (!wait(&ctrl->p_full[0], par(4))) { ok = false; break; }
+                        flip(4);
+                        ptx::tc_fence_after();
+                        pv_products(0, vs, j == 0);
+                        if (j == nA - 1) ptx::mma_commit(&ctrl->o_final[0]);
+                        if (j + 1 < nA) {
+                            s_products(0, ks);
+                            if (j + 2 == nA) ptx::mma_commit(&ctrl->q_empty[0]);
+                        }
+                    }
+                    if (j < nB) {
+                        if (!wait(&ctrl->p_full[1], par(5))) { ok = false; break; }
+                        flip(5);
+                        ptx::tc_fence_after();
+                        pv_products(1, vs, j == 0);
+                        if (j == nB - 1) ptx::mma_commit(&ctrl->o_final[1]);
+                        if (j + 1 < nB) {
+                            s_products(1, ks);
+                            if (j + 2 == nB) ptx::mma_commit(&ctrl->q_empty[1]);
+                        }
+                    }
                     // the last V slot of the item is released by tile B's epilogue, which stages
                     // its output there
-                    if (j + 1 < nmax) {
+                    if (more) {
                         ptx::mma_commit(&ctrl->v_empty[vs]);
-                        ptx::mma_commit(&ctrl->k_empty[(gj + 1) % KS]);
+                        ptx::mma_commit(&ctrl->k_empty[ks]);
+                        if (++ks == KS) { ks = 0; flip(0); }
                     }
+                    if (++vs == VS) { vs = 0; flip(1); }
                 }
-                g += nmax;
-                uA += nA;
-                uB += nB;
             }
             ptx::mma_commit(&ctrl->final_mma);
             if (!ptx::mbar_wait_quiet(&ctrl->final_mma, 0, kWaitLimitNs)) atomicOr(a.flags, kFlagWaitTimeout);
