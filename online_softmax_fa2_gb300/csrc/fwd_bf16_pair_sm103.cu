@@ -121,24 +121,44 @@ __device__ __forceinline__ Item next_item(const Args &a, const DropArgs &dr, int
     return none;
 }
 
-// Dropout (training forward): the 128 keep bits of a row for one key tile, as four 32-bit
-// words (bit t of word w = key 32w + t of the tile), applied to p after the row sum has taken
-// it: dropped weights 0, kept ones as they are (the 1 / (1 - dropout_p) of the kept ones is
-// applied once, to the row's output, in the epilogue).
-__device__ __forceinline__ void apply_keep(float (&x)[BK], const uint4 &keep) {
+// Dropout (training forward): store_p with the row's 128 keep bits for the key tile applied as
+// P is rounded and packed (bit t of word w = key 32w + t of the tile; dropped weights 0, kept
+// ones as they are: the 1 / (1 - dropout_p) of the kept ones is applied once, to the row's
+// output, in the epilogue).  The bits are needed only while the row's values are already
+// leaving registers, which keeps the softmax threads from spilling.
+__device__ __forceinline__ void store_p_keep(uint32_t taddr, const float (&x)[BK], const uint4 &keep) {
     const uint32_t w[4] = {keep.x, keep.y, keep.z, keep.w};
 #pragma unroll
-    for (int k = 0; k < BK; ++k) x[k] = ((w[k >> 5] >> (k & 31)) & 1u) ? x[k] : 0.f;
+    for (int cc = 0; cc < BK / 64; ++cc) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const int k = cc * 64 + 2 * t;
+            const float lo = ((w[k >> 5] >> (k & 31)) & 1u) ? x[k] : 0.f;
+            const float hi = ((w[(k + 1) >> 5] >> ((k + 1) & 31)) & 1u) ? x[k + 1] : 0.f;
+            pk[t] = ptx::pack_bf16x2(lo, hi);
+        }
+        ptx::tmem_st32(taddr + cc * 32, pk);
+    }
+    ptx::tmem_st_wait();
 }
 
 __device__ __forceinline__ uint4 ld_keep(const uint8_t *p) {
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// The next tile's keep bits are prefetched into L1 and loaded only where they are applied, so
+// that no register holds them through the softmax.
+__device__ __forceinline__ void prefetch_keep(const uint8_t *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // kPartial: write each row's state (m, l, u) over the kernel's keys to dr.part ([B, H, Nq,
 // 2 + DV] fp32; m the row's reference in natural-log units, l and u measured against it;
 // (-inf, 0, 0) for a row that sees no key) instead of o and lse.
-template <int DK, int DV, bool kBias, bool kDrop, bool kPartial>
+// kDrop: 0 no dropout, 1 keep bits from a mask, 2 keep bits drawn in-kernel (separate
+// instantiations, so that neither path holds the other's state in registers).
+template <int DK, int DV, bool kBias, int kDrop, bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -464,14 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t *keep_row = nullptr;
             uint4 keep = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t bh = (uint32_t)(it.b * a.H + it.h);
-            if constexpr (kDrop) {
+            if constexpr (kDrop == 2) {
+                if (i < a.Nq) keep = rng::keep128((uint32_t)i, 0u, bh, dr.offset, dr.seed_lo, dr.seed_hi, dr.p8x4);
+            } else if constexpr (kDrop == 1) {
                 if (i < a.Nq) {
-                    if (dr.rng) {
-                        keep = rng::keep128((uint32_t)i, 0u, bh, dr.offset, dr.seed_lo, dr.seed_hi, dr.p8x4);
-                    } else {
-                        keep_row = dr.dmask + it.b * dr.dms0 + it.h * dr.dms1 + (long long)i * dr.dms2;
-                        keep = ld_keep(keep_row);
-                    }
+                    keep_row = dr.dmask + it.b * dr.dms0 + it.h * dr.dms1 + (long long)i * dr.dms2;
+                    prefetch_keep(keep_row);
                 }
             }
             for (int j = 0; j < nX; ++j) {
@@ -489,9 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = update_max(mt, m_run, rescale);
                 const float lsum = tile_exp<kBias>(x, c, m_run);
                 l_run = fmaf(alpha, l_run, lsum);
-                if constexpr (kDrop) {  // the row sum keeps the undropped weights
-                    apply_keep(x, keep);
-                }
+
                 if (__any_sync(0xffffffffu, rescale)) scale_o<DV>(lane_addr + o_col, alpha);
                 // value rows past n inside this tile may hold anything: the warpgroup of the
                 // first query tile that uses V_j zeroes them before its product reads V_j
@@ -504,13 +520,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         zero_v_row<DV>(smem + L::kVOff + (gj % VS) * L::kVBytes, r);
                     ptx::fence_proxy_async_smem();
                 }
-                store_p(lane_addr + s_col, x);
+                // dropout: the row sum above kept the undropped weights; P drops them
+                if constexpr (kDrop == 1) {
+                    store_p_keep(lane_addr + s_col, x,
+                                 keep_row ? ld_keep(keep_row + j * (BK / 8)) : make_uint4(0u, 0u, 0u, 0u));
+                } else if constexpr (kDrop == 2) {
+                    store_p_keep(lane_addr + s_col, x, keep);
+                } else {
+                    store_p(lane_addr + s_col, x);
+                }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&ctrl->p_full[X]);
                 if (kBias && j + 1 < nX) load_bias(bias_row, bias_vec, kv0 + BK, it.n, x);
-                if constexpr (kDrop) {
-                    if (keep_row && j + 1 < nX) keep = ld_keep(keep_row + (j + 1) * (BK / 8));
-                    if (dr.rng && i < a.Nq && j + 1 < nX)
+                if constexpr (kDrop == 1) {
+                    if (keep_row && j + 1 < nX) prefetch_keep(keep_row + (j + 1) * (BK / 8));
+                } else if constexpr (kDrop == 2) {
+                    if (i < a.Nq && j + 1 < nX)
                         keep = rng::keep128((uint32_t)i, (uint32_t)(kv0 + BK), bh, dr.offset, dr.seed_lo, dr.seed_hi,
                                             dr.p8x4);
                 }
@@ -543,12 +568,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Q_B can load meanwhile; the store releases that slot.  With dv > dk the Q buffer
             // is too small and tile A writes its rows directly.
             if (!kStageA && X == 0) {
-                write_row<DV>(lane_addr + o_col, l_run, m_run, out_row(), out_lse(), kDrop ? dr.inv_keep : 1.f);
+                write_row<DV>(lane_addr + o_col, l_run, m_run, out_row(), out_lse(), kDrop != 0 ? dr.inv_keep : 1.f);
                 ptx::tc_fence_before();
             } else {
                 const int sl = (g + it.nmax - 1) % VS;
                 uint8_t *stage = X ? smem + L::kVOff + sl * L::kVBytes : smem;
-                stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, out_lse(), kDrop ? dr.inv_keep : 1.f);
+                stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, out_lse(), kDrop != 0 ? dr.inv_keep : 1.f);
                 ptx::tc_fence_before();
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&ctrl->o_staged[X]);
@@ -579,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int DK, int DV, bool kBias, bool kDrop, bool kPartial = false>
+template <int DK, int DV, bool kBias, int kDrop, bool kPartial = false>
 attn_status_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                        const CUtensorMap &mo, const Args &a, const DropArgs &dr, cudaStream_t s) {
     const int smem = Layout<DK, DV>::kBytes;
@@ -605,20 +630,23 @@ attn_status_t launch_fwd_bf16_pair(const CUtensorMap &mq, const CUtensorMap &mk,
                                    cudaStream_t s) {
     if (dr.part) {  // partial states: dk == dv in {64, 128}, no dropout (checked by the caller)
         if (dk == 128 && dv == 128)
-            return bias ? launch_t<128, 128, true, false, true>(mq, mk, mv, mo, a, dr, s)
-                        : launch_t<128, 128, false, false, true>(mq, mk, mv, mo, a, dr, s);
+            return bias ? launch_t<128, 128, true, 0, true>(mq, mk, mv, mo, a, dr, s)
+                        : launch_t<128, 128, false, 0, true>(mq, mk, mv, mo, a, dr, s);
         if (dk == 64 && dv == 64)
-            return bias ? launch_t<64, 64, true, false, true>(mq, mk, mv, mo, a, dr, s)
-                        : launch_t<64, 64, false, false, true>(mq, mk, mv, mo, a, dr, s);
+            return bias ? launch_t<64, 64, true, 0, true>(mq, mk, mv, mo, a, dr, s)
+                        : launch_t<64, 64, false, 0, true>(mq, mk, mv, mo, a, dr, s);
         return fail(ATTN_ERR_UNSUPPORTED, "partial states need dk == dv in {64, 128} (dk=%d dv=%d)", dk, dv);
     }
 #define ATTN_PAIR_CASE(DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_) {                                                              \
-        if (dr.dmask || dr.rng)                                                                \
-            return bias ? launch_t<DK_, DV_, true, true>(mq, mk, mv, mo, a, dr, s)                 \
-                        : launch_t<DK_, DV_, false, true>(mq, mk, mv, mo, a, dr, s);               \
-        return bias ? launch_t<DK_, DV_, true, false>(mq, mk, mv, mo, a, dr, s)                    \
-                    : launch_t<DK_, DV_, false, false>(mq, mk, mv, mo, a, dr, s);                  \
+        if (dr.rng)                                                                            \
+            return bias ? launch_t<DK_, DV_, true, 2>(mq, mk, mv, mo, a, dr, s)                    \
+                        : launch_t<DK_, DV_, false, 2>(mq, mk, mv, mo, a, dr, s);                  \
+        if (dr.dmask)                                                                          \
+            return bias ? launch_t<DK_, DV_, true, 1>(mq, mk, mv, mo, a, dr, s)                    \
+                        : launch_t<DK_, DV_, false, 1>(mq, mk, mv, mo, a, dr, s);                  \
+        return bias ? launch_t<DK_, DV_, true, 0>(mq, mk, mv, mo, a, dr, s)                        \
+                    : launch_t<DK_, DV_, false, 0>(mq, mk, mv, mo, a, dr, s);                      \
     }
     ATTN_PAIR_CASE(128, 128)
     ATTN_PAIR_CASE(64, 64)
