@@ -37,7 +37,29 @@ struct Args {
     long long bs0, bs1, bs2;
     const int *kv_lens;
     uint32_t *flags;
+    // division by B * H and by H as a multiply-high and two shifts (fill_divisors)
+    uint32_t div_bhn_m, div_h_m;
+    int div_bhn_s, div_h_s;  // first shift | second shift << 8
 };
+
+// The multiply-high division of Granlund and Montgomery ("Division by invariant integers using
+// multiplication", PLDI 1994, section 4), exact for every 32-bit dividend: for a divisor d >= 1
+// with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 and n / d = (t + ((n - t) >> s1)) >> s2
+// where t = umulhi(m, n), s1 = min(l, 1), s2 = max(l - 1, 0).
+inline void fast_div_params(uint32_t d, uint32_t &m, int &s) {
+    int l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d) + 1;
+    s = (l < 1 ? l : 1) | ((l > 1 ? l - 1 : 0) << 8);
+}
+inline void fill_divisors(Args &a) {
+    fast_div_params((uint32_t)(a.B * a.H), a.div_bhn_m, a.div_bhn_s);
+    fast_div_params((uint32_t)a.H, a.div_h_m, a.div_h_s);
+}
+__device__ __forceinline__ uint32_t div_fast(uint32_t n, uint32_t m, int s) {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> (s & 255))) >> (s >> 8);
+}
 
 // Options beyond the plain operator, in a kernel argument of their own so that the kernels
 // that use none keep their argument block (and their register allocation):

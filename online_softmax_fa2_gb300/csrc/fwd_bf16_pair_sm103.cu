@@ -82,11 +82,12 @@ struct Item {
 template <bool kShard = false>
 __device__ __forceinline__ Item decode_item(const Args &a, const DropArgs &dr, int k, bool report) {
     Item it;
-    const int bhn = a.B * a.H;
-    const int blk = a.n_items - 1 - k / bhn;  // later query blocks see more keys: first
-    const int bh = k % bhn;
-    it.b = bh / a.H;
-    it.h = bh % a.H;
+    // k / (B H) and bh / H by multiply-high (every role decodes at every item boundary)
+    const int kq = (int)div_fast((uint32_t)k, a.div_bhn_m, a.div_bhn_s);
+    const int blk = a.n_items - 1 - kq;  // later query blocks see more keys: first
+    const int bh = k - kq * (a.B * a.H);
+    it.b = (int)div_fast((uint32_t)bh, a.div_h_m, a.div_h_s);
+    it.h = bh - it.b * a.H;
     it.q0 = blk * 2 * BQ;
     if constexpr (kShard) {
         const int len = seq_len(a, it.b, report && blk == 0 && it.h == 0, dr.Nk_tot);  // the whole sequence's

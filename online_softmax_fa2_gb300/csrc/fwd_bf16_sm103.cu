@@ -568,6 +568,7 @@ attn_status_t launch_fwd_bf16(const attn_fwd_params_t &p, cudaStream_t s) {
     Args a;
     a.B = (int)p.B; a.H = (int)p.H; a.Nq = (int)p.Nq; a.Nk = (int)p.Nk; a.causal = p.causal;
     a.n_items = (int)((p.Nq + (pair ? 2 * BQ : BQ) - 1) / (pair ? 2 * BQ : BQ));
+    fill_divisors(a);
     a.scale_log2 = p.scale * kLog2e;
     a.o = static_cast<__nv_bfloat16 *>(p.o);
     a.os0 = p.o_stride[0]; a.os1 = p.o_stride[1]; a.os2 = p.o_stride[2];
@@ -612,6 +613,7 @@ attn_status_t launch_fwd_bf16_partial(const attn_fwd_params_t &p, int64_t key_of
     Args a;
     a.B = (int)p.B; a.H = (int)p.H; a.Nq = (int)p.Nq; a.Nk = (int)p.Nk; a.causal = p.causal;
     a.n_items = (int)((p.Nq + 2 * BQ - 1) / (2 * BQ));
+    fill_divisors(a);
     a.scale_log2 = p.scale * kLog2e;
     a.o = nullptr;
     a.os0 = a.os1 = a.os2 = 0;
