@@ -56,7 +56,10 @@ struct Layout {
     static constexpr int kQBytes = (DK / 64) * kPanelBytes;  // one query tile
     static constexpr int kKBytes = (DK / 64) * kPanelBytes;
     static constexpr int kVBytes = (DV / 64) * kPanelBytes;
-    static constexpr int kFixed = 2 * kQBytes + (int)sizeof(Ctrl) + 1024;
+    // tile A's output is staged in a buffer of its own, so that Q_A is released by its last
+    // S product alone and the next item's Q_A loads while the item's last key tiles run
+    static constexpr int kStageBytes = kVBytes;
+    static constexpr int kFixed = 2 * kQBytes + kStageBytes + (int)sizeof(Ctrl) + 1024;
     // as many K stages as fit with 2 V stages (at most 4), then V stages likewise
     static constexpr int kKStages =
         (kFixed + 4 * kKBytes + 2 * kVBytes <= kSmemMax) ? 4
@@ -66,7 +69,8 @@ struct Layout {
         : (kFixed + kKStages * kKBytes + 3 * kVBytes <= kSmemMax) ? 3 : 2;
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kKStages * kKBytes;
-    static constexpr int kDataBytes = kVOff + kVStages * kVBytes;
+    static constexpr int kStageOff = kVOff + kVStages * kVBytes;
+    static constexpr int kDataBytes = kStageOff + kStageBytes;
     static constexpr int kBytes = kDataBytes + (int)sizeof(Ctrl) + 1024;
     static_assert(kBytes <= kSmemMax, "shared memory budget");
 };
@@ -167,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_o, const Args a, const DropArgs dr) {
     using L = Layout<DK, DV>;
     constexpr int KS = L::kKStages, VS = L::kVStages;
-    constexpr bool kStageA = DV <= DK;  // tile A's output fits in its Q buffer
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -182,9 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(&ctrl->q_full[t], 1);
-            // Q_A is released by its last S product and by tile A's output store, which is
-            // staged in the same buffer when it fits (dv <= dk); Q_B by its last S product
-            ptx::mbar_init(&ctrl->q_empty[t], (t == 0 && kStageA) ? 2 : 1);
+            ptx::mbar_init(&ctrl->q_empty[t], 1);  // released by the item's last S_t
             ptx::mbar_init(&ctrl->o_staged[t], BQ);
             ptx::mbar_init(&ctrl->s_full[t], 1);
             ptx::mbar_init(&ctrl->p_full[t], BQ);
@@ -552,7 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_before();
                 if (r == 0) {
                     if (X) ptx::mbar_arrive(&ctrl->v_empty[(g + it.nmax - 1) % VS]);
-                    else if (kStageA) ptx::mbar_arrive(&ctrl->q_empty[0]);
                 }
                 g += it.nmax;
                 u += nX;
@@ -562,18 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // divide once and store the row; the next item's first P V product overwrites O_X
             // only after this thread's next P hand-off, which follows these TMEM loads
             // Each tile's rows go through shared memory in the swizzled box layout, and one
-            // thread stores the tile with TMA.  Tile A stages in its Q buffer (its last S
-            // product has completed), which the store then releases to the producer.  Tile B
-            // finishes last (it sees at least as many key tiles as tile A) and stages in the
-            // item's last V slot, whose products have all completed, so that the next item's
-            // Q_B can load meanwhile; the store releases that slot.  With dv > dk the Q buffer
-            // is too small and tile A writes its rows directly.
-            if (!kStageA && X == 0) {
-                write_row<DV>(lane_addr + o_col, l_run, m_run, out_row(), out_lse(), kDrop != 0 ? dr.inv_keep : 1.f);
-                ptx::tc_fence_before();
-            } else {
+            // thread stores the tile with TMA.  Tile A stages in a buffer of its own (Q_A has
+            // been released by its last S product, so the next item's Q_A is already loading).
+            // Tile B finishes last (it sees at least as many key tiles as tile A) and stages in
+            // the item's last V slot, whose products have all completed, so that the next
+            // item's Q_B can load meanwhile; the store releases that slot.
+            {
                 const int sl = (g + it.nmax - 1) % VS;
-                uint8_t *stage = X ? smem + L::kVOff + sl * L::kVBytes : smem;
+                uint8_t *stage = X ? smem + L::kVOff + sl * L::kVBytes : smem + L::kStageOff;
                 stage_row<DV>(lane_addr + o_col, l_run, m_run, stage, r, out_lse(), kDrop != 0 ? dr.inv_keep : 1.f);
                 ptx::tc_fence_before();
                 ptx::fence_proxy_async_smem();
@@ -587,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::bulk_commit();
                         ptx::bulk_wait_read();
                     }
-                    ptx::mbar_arrive(X ? &ctrl->v_empty[sl] : &ctrl->q_empty[0]);
+                    if (X) ptx::mbar_arrive(&ctrl->v_empty[sl]);
                 }
             }
             g += it.nmax;
